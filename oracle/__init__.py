@@ -1,0 +1,11 @@
+"""fp64 CPU oracle (test infrastructure only; see fa_oracle.py's header)."""
+
+from .fa_oracle import (  # noqa: F401
+    backward,
+    bwd_preprocess,
+    forward,
+    kv_head,
+    unit_backward,
+    unit_forward,
+    unit_scores,
+)

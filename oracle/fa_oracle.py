@@ -1,0 +1,211 @@
+"""fp64 CPU oracle for scaled-dot-product attention, forward and backward.
+
+TEST INFRASTRUCTURE ONLY.  Nothing on the product path may import, call or
+execute this module: only ``tests/``, ``__graft_entry__.smoke()`` and the
+``cpu_baseline`` / ``--impl reference`` legs of ``bench.py`` use it.  It shares
+no code with the CUDA path and imports nothing from the package.
+
+What it computes, written out from its plain definition (no tiling, no online
+softmax, no fusion):
+
+* Forward, per (batch b, query head h), following the core-formula section of
+  "使用 TileLang 在 AMD GPU 上快速开发高性能 Flash Attention" (score
+  computation, optional causal mask, softmax, output) and the PyTorch
+  reference function described on the same page:
+
+      S = Q_bh K_{b,hk}^T / sqrt(D)              (full L x L matrix)
+      S[i, j] = -inf  for j > i                   (causal, top-left aligned)
+      m_i = max_j S_ij
+      P_ij = exp(S_ij - m_i) / sum_j exp(S_ij - m_i)   (two-pass softmax)
+      O = P V_{b,hk}                              (explicit matmul)
+
+  with the grouped-query head map hk = h // (H // Hkv): the page's kernel
+  reads the K/V head whose index is the query head divided by the group
+  size, and its PyTorch reference repeats each K/V head group-size times
+  along the head axis, which is the same map.
+
+* LSE (the pages only name the tensor ``lse`` as an input of the backward
+  kernel in "TileLang与机器学习训练：反向传播算子优化案例", section
+  算子拆分与流水线设计): reading taken here is the natural-log log-sum-exp of
+  the scaled, masked scores, LSE_i = m_i + ln sum_j exp(S_ij - m_i).
+
+* Backward preprocess, same page and section: Delta_i = sum_d O_id dO_id.
+  The printed snippet multiplies an O block by a transposed dO block and
+  row-sums the product, which taken literally mixes different rows; the
+  reading used here is the per-row dot product that the softmax gradient
+  needs.
+
+* Backward (the page elides every step after the dV product): the analytic
+  gradient of O = softmax(S) V,
+
+      dV = P^T dO,  dP = dO V^T,  dS = P o (dP - Delta 1^T),
+      dQ = dS K / sqrt(D),  dK = dS^T Q / sqrt(D),
+
+  with dK and dV of a KV head summed over the query heads of its group (what
+  differentiating through the head repeat gives).
+
+All arithmetic is numpy float64; matmul and exp are library primitives.  For
+very long sequences the per-unit functions may process query rows in panels:
+each row's softmax still sees all of its keys, so the result is the same
+computation, only with the row loop split.
+"""
+
+from __future__ import annotations
+
+import numpy as np
+
+__all__ = [
+    "kv_head",
+    "unit_scores",
+    "unit_forward",
+    "unit_backward",
+    "forward",
+    "backward",
+    "bwd_preprocess",
+]
+
+
+def kv_head(h: int, H: int, Hkv: int) -> int:
+    """K/V head that query head ``h`` reads (grouped-query map h -> h // groups)."""
+    if H % Hkv != 0:
+        raise ValueError(f"H={H} is not a multiple of Hkv={Hkv}")
+    return h // (H // Hkv)
+
+
+def _as64(x) -> np.ndarray:
+    a = np.asarray(x, dtype=np.float64)
+    return a
+
+
+def unit_scores(q_bh: np.ndarray, k_bh: np.ndarray, causal: bool,
+                row0: int = 0) -> np.ndarray:
+    """Scaled, masked score rows S[row0:row0+n, :] for one (b, h).
+
+    q_bh: [n, D] query rows row0..row0+n-1; k_bh: [L, D] all keys.
+    Causal masking is top-left aligned: key j is visible to query i iff j <= i.
+    """
+    n, D = q_bh.shape
+    L = k_bh.shape[0]
+    S = (q_bh @ k_bh.T) / np.sqrt(D)
+    if causal:
+        i = np.arange(row0, row0 + n)[:, None]
+        j = np.arange(L)[None, :]
+        S = np.where(j > i, -np.inf, S)
+    return S
+
+
+def _softmax_rows(S: np.ndarray):
+    """Two-pass row softmax: returns P, row max m, row sum of exp(S - m)."""
+    m = S.max(axis=1, keepdims=True)
+    E = np.exp(S - m)
+    s = E.sum(axis=1, keepdims=True)
+    return E / s, m[:, 0], s[:, 0]
+
+
+def unit_forward(q_bh, k_bh, v_bh, causal: bool, rows=None, panel: int = 4096):
+    """O and LSE rows of one (b, h).
+
+    q_bh [L, D], k_bh / v_bh [L, D] (already the K/V head this query head
+    reads).  ``rows`` (optional int array) restricts the output to those query
+    rows; the keys are always all L.  Returns (O [n, D], LSE [n]).
+    """
+    q_bh, k_bh, v_bh = _as64(q_bh), _as64(k_bh), _as64(v_bh)
+    L = q_bh.shape[0]
+    rows = np.arange(L) if rows is None else np.asarray(rows)
+    outs_o, outs_l = [], []
+    for p0 in range(0, len(rows), panel):
+        r = rows[p0:p0 + panel]
+        S = (q_bh[r] @ k_bh.T) / np.sqrt(q_bh.shape[1])
+        if causal:
+            S = np.where(np.arange(L)[None, :] > r[:, None], -np.inf, S)
+        P, m, s = _softmax_rows(S)
+        outs_o.append(P @ v_bh)
+        outs_l.append(m + np.log(s))
+    if not outs_o:
+        return np.zeros((0, q_bh.shape[1])), np.zeros((0,))
+    return np.concatenate(outs_o), np.concatenate(outs_l)
+
+
+def unit_backward(q_bh, k_bh, v_bh, do_bh, causal: bool, panel: int = 4096):
+    """Gradients of one (b, h) pair against its K/V head.
+
+    Returns (dQ [L, D], dK [L, D], dV [L, D], Delta [L], O [L, D], LSE [L]).
+    The oracle recomputes its own O and Delta; nothing comes from a kernel.
+    """
+    q_bh, k_bh, v_bh, do_bh = (_as64(x) for x in (q_bh, k_bh, v_bh, do_bh))
+    L, D = q_bh.shape
+    inv = 1.0 / np.sqrt(D)
+    dq = np.zeros((L, D))
+    dk = np.zeros((L, D))
+    dv = np.zeros((L, D))
+    o = np.zeros((L, D))
+    lse = np.zeros((L,))
+    delta = np.zeros((L,))
+    for r0 in range(0, L, panel):
+        r = np.arange(r0, min(L, r0 + panel))
+        S = (q_bh[r] @ k_bh.T) * inv
+        if causal:
+            S = np.where(np.arange(L)[None, :] > r[:, None], -np.inf, S)
+        P, m, s = _softmax_rows(S)
+        O = P @ v_bh
+        o[r] = O
+        lse[r] = m + np.log(s)
+        dO = do_bh[r]
+        dl = (O * dO).sum(axis=1)               # Delta_i = sum_d O_id dO_id
+        delta[r] = dl
+        dv += P.T @ dO                          # dV = P^T dO
+        dP = dO @ v_bh.T                        # dP = dO V^T
+        dS = P * (dP - dl[:, None])             # dS = P o (dP - Delta)
+        dq[r] = (dS @ k_bh) * inv               # dQ = dS K / sqrt(D)
+        dk += (dS.T @ q_bh[r]) * inv            # dK = dS^T Q / sqrt(D)
+    return dq, dk, dv, delta, o, lse
+
+
+def forward(q, k, v, causal: bool):
+    """Full forward over BSHD tensors.
+
+    q [B, L, H, D]; k, v [B, L, Hkv, D].  Returns O [B, L, H, D] and
+    LSE [B, H, L] (float64).
+    """
+    q, k, v = _as64(q), _as64(k), _as64(v)
+    B, L, H, D = q.shape
+    Hkv = k.shape[2]
+    o = np.zeros((B, L, H, D))
+    lse = np.zeros((B, H, L))
+    for b in range(B):
+        for h in range(H):
+            hk = kv_head(h, H, Hkv)
+            o[b, :, h, :], lse[b, h, :] = unit_forward(
+                q[b, :, h, :], k[b, :, hk, :], v[b, :, hk, :], causal)
+    return o, lse
+
+
+def bwd_preprocess(o, do):
+    """Delta[b, h, i] = sum_d O[b, i, h, d] * dO[b, i, h, d], as [B, H, L]."""
+    o, do = _as64(o), _as64(do)
+    return np.einsum("blhd,blhd->bhl", o, do)
+
+
+def backward(q, k, v, do, causal: bool):
+    """Full backward over BSHD tensors.
+
+    Returns dQ [B, L, H, D], dK [B, L, Hkv, D], dV [B, L, Hkv, D],
+    Delta [B, H, L] (from the oracle's own O).
+    """
+    q, k, v, do = _as64(q), _as64(k), _as64(v), _as64(do)
+    B, L, H, D = q.shape
+    Hkv = k.shape[2]
+    dq = np.zeros((B, L, H, D))
+    dk = np.zeros((B, L, Hkv, D))
+    dv = np.zeros((B, L, Hkv, D))
+    delta = np.zeros((B, H, L))
+    for b in range(B):
+        for h in range(H):
+            hk = kv_head(h, H, Hkv)
+            gq, gk, gv, dl, _, _ = unit_backward(
+                q[b, :, h, :], k[b, :, hk, :], v[b, :, hk, :], do[b, :, h, :], causal)
+            dq[b, :, h, :] = gq
+            dk[b, :, hk, :] += gk                 # group heads sum into their KV head
+            dv[b, :, hk, :] += gv
+            delta[b, h, :] = dl
+    return dq, dk, dv, delta

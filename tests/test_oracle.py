@@ -1,0 +1,406 @@
+"""Pins for the fp64 oracle, checked against what the mathematics fixes.
+
+The pages print no worked numeric example, so every pin here is a closed form,
+an invariant, an independent brute-force or library computation, or a finite
+difference.  ``test_planted_mistakes_are_caught`` plants plausible mistakes in
+a copy of the oracle and checks that at least one pin fails for each.
+"""
+
+import math
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import fa_oracle as orc
+from tiled_attention_fa_gb300.inputs import make_qkv
+
+pytestmark = pytest.mark.filterwarnings("ignore::RuntimeWarning")
+
+
+def rnd(shape, seed):
+    return np.random.default_rng(seed).standard_normal(shape)
+
+
+# ---------------------------------------------------------------- forward pins
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_softmax_rows_sum_to_one(causal):
+    # With D = L and V = identity, O is the probability matrix itself.
+    L = 24
+    q, k = rnd((L, L), 1), rnd((L, L), 2)
+    P, _ = orc.unit_forward(q, k, np.eye(L), causal)
+    assert np.all(P >= 0)
+    np.testing.assert_allclose(P.sum(axis=1), 1.0, atol=1e-12)
+    if causal:
+        assert np.all(P[np.triu_indices(L, 1)] == 0.0)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_constant_values_give_that_value(causal):
+    L, D = 37, 16
+    v_row = rnd((D,), 3)
+    o, _ = orc.unit_forward(rnd((L, D), 4) * 3, rnd((L, D), 5) * 3,
+                            np.tile(v_row, (L, 1)), causal)
+    np.testing.assert_allclose(o, np.tile(v_row, (L, 1)), atol=1e-12)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_zero_queries_give_mean_of_values(causal):
+    L, D = 29, 8
+    v = rnd((L, D), 6)
+    o, lse = orc.unit_forward(np.zeros((L, D)), rnd((L, D), 7), v, causal)
+    if causal:
+        want = np.cumsum(v, axis=0) / np.arange(1, L + 1)[:, None]
+        want_lse = np.log(np.arange(1, L + 1))
+    else:
+        want = np.tile(v.mean(axis=0), (L, 1))
+        want_lse = np.full(L, math.log(L))
+    np.testing.assert_allclose(o, want, atol=1e-12)
+    np.testing.assert_allclose(lse, want_lse, atol=1e-12)
+
+
+def test_causal_first_row_is_first_value():
+    L, D = 20, 8
+    q, k, v = rnd((L, D), 8), rnd((L, D), 9), rnd((L, D), 10)
+    o, lse = orc.unit_forward(q, k, v, True)
+    np.testing.assert_allclose(o[0], v[0], atol=1e-14)
+    assert lse[0] == pytest.approx(q[0] @ k[0] / math.sqrt(D), abs=1e-13)
+
+
+def test_two_key_closed_form():
+    # Scores [x, 0] give weights [sigmoid(x), 1 - sigmoid(x)] and LSE ln(e^x + 1).
+    D = 4
+    for x in (-3.0, 0.0, 0.7, 5.0):
+        q = np.array([[2.0 * x, 0, 0, 0]])            # q.k0 / sqrt(4) = x
+        k = np.array([[1.0, 0, 0, 0], [0, 0, 0, 0]])
+        v = np.array([[1.0, 2, 3, 4], [-1.0, 0, 5, 0]])
+        o, lse = orc.unit_forward(q, k, v, False)
+        p = 1.0 / (1.0 + math.exp(-x))
+        np.testing.assert_allclose(o[0], p * v[0] + (1 - p) * v[1], atol=1e-14)
+        assert lse[0] == pytest.approx(math.log(math.exp(x) + 1.0), abs=1e-14)
+
+
+def test_permuting_keys_and_values_together():
+    L, D = 33, 16
+    q, k, v = rnd((L, D), 11), rnd((L, D), 12), rnd((L, D), 13)
+    perm = np.random.default_rng(14).permutation(L)
+    o1, l1 = orc.unit_forward(q, k, v, False)
+    o2, l2 = orc.unit_forward(q, k[perm], v[perm], False)
+    np.testing.assert_allclose(o1, o2, atol=1e-12)
+    np.testing.assert_allclose(l1, l2, atol=1e-12)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_shifting_every_key(causal):
+    L, D = 25, 8
+    q, k, v = rnd((L, D), 15), rnd((L, D), 16), rnd((L, D), 17)
+    c = rnd((D,), 18)
+    o1, l1 = orc.unit_forward(q, k, v, causal)
+    o2, l2 = orc.unit_forward(q, k + c, v, causal)
+    np.testing.assert_allclose(o1, o2, atol=1e-12)
+    np.testing.assert_allclose(l2 - l1, q @ c / math.sqrt(D), atol=1e-12)
+
+
+def brute_force_forward(q, k, v, causal):
+    """Straight-line loops over scalars, independent of the oracle's numpy code."""
+    B, L, H, D = q.shape
+    Hkv = k.shape[2]
+    o = np.zeros((B, L, H, D))
+    lse = np.zeros((B, H, L))
+    for b in range(B):
+        for h in range(H):
+            hk = h // (H // Hkv)
+            for i in range(L):
+                s = []
+                for j in range(L):
+                    if causal and j > i:
+                        continue
+                    s.append((j, sum(q[b, i, h, d] * k[b, j, hk, d] for d in range(D)) / math.sqrt(D)))
+                mx = max(x for _, x in s)
+                z = sum(math.exp(x - mx) for _, x in s)
+                lse[b, h, i] = mx + math.log(z)
+                for d in range(D):
+                    o[b, i, h, d] = sum(math.exp(x - mx) / z * v[b, j, hk, d] for j, x in s)
+    return o, lse
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("H,Hkv", [(1, 1), (4, 2)])
+def test_brute_force_small(causal, H, Hkv):
+    B, L, D = 2, 7, 5
+    q, k, v = rnd((B, L, H, D), 19), rnd((B, L, Hkv, D), 20), rnd((B, L, Hkv, D), 21)
+    o, lse = orc.forward(q, k, v, causal)
+    ob, lb = brute_force_forward(q, k, v, causal)
+    np.testing.assert_allclose(o, ob, atol=1e-12)
+    np.testing.assert_allclose(lse, lb, atol=1e-12)
+
+
+def torch_reference(q, k, v, do, causal):
+    """torch's own float64 attention and autograd, a separately written library path."""
+    H, Hkv = q.shape[2], k.shape[2]
+    g = H // Hkv
+    tq = torch.tensor(q).permute(0, 2, 1, 3).requires_grad_()
+    tk = torch.tensor(k).permute(0, 2, 1, 3).requires_grad_()
+    tv = torch.tensor(v).permute(0, 2, 1, 3).requires_grad_()
+    kk = tk.repeat_interleave(g, dim=1)
+    vv = tv.repeat_interleave(g, dim=1)
+    out = torch.nn.functional.scaled_dot_product_attention(tq, kk, vv, is_causal=causal)
+    out.backward(torch.tensor(do).permute(0, 2, 1, 3))
+    f = lambda t: t.detach().permute(0, 2, 1, 3).numpy()
+    return f(out), f(tq.grad), f(tk.grad), f(tv.grad)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("H,Hkv", [(2, 2), (4, 1)])
+def test_matches_torch_float64_reference(causal, H, Hkv):
+    B, L, D = 2, 45, 16
+    q, k, v, do = (rnd((B, L, h, D), s) for h, s in ((H, 22), (Hkv, 23), (Hkv, 24), (H, 25)))
+    o, _ = orc.forward(q, k, v, causal)
+    dq, dk, dv, _ = orc.backward(q, k, v, do, causal)
+    to, tdq, tdk, tdv = torch_reference(q, k, v, do, causal)
+    for a, b in ((o, to), (dq, tdq), (dk, tdk), (dv, tdv)):
+        np.testing.assert_allclose(a, b, atol=1e-11, rtol=1e-9)
+
+
+def test_gqa_equals_mha_on_repeated_heads():
+    B, L, H, Hkv, D = 1, 19, 6, 2, 8
+    q, k, v, do = rnd((B, L, H, D), 26), rnd((B, L, Hkv, D), 27), rnd((B, L, Hkv, D), 28), rnd((B, L, H, D), 29)
+    kr, vr = np.repeat(k, H // Hkv, axis=2), np.repeat(v, H // Hkv, axis=2)
+    for causal in (False, True):
+        o1, l1 = orc.forward(q, k, v, causal)
+        o2, l2 = orc.forward(q, kr, vr, causal)
+        np.testing.assert_allclose(o1, o2, atol=1e-14)
+        np.testing.assert_allclose(l1, l2, atol=1e-14)
+        dq1, dk1, dv1, _ = orc.backward(q, k, v, do, causal)
+        dq2, dk2, dv2, _ = orc.backward(q, kr, vr, do, causal)
+        np.testing.assert_allclose(dq1, dq2, atol=1e-13)
+        g = H // Hkv
+        np.testing.assert_allclose(dk1, dk2.reshape(B, L, Hkv, g, D).sum(axis=3), atol=1e-13)
+        np.testing.assert_allclose(dv1, dv2.reshape(B, L, Hkv, g, D).sum(axis=3), atol=1e-13)
+
+
+# ---------------------------------------------------------------- backward pins
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_gradients_match_central_finite_differences(causal):
+    B, L, H, Hkv, D = 1, 5, 2, 1, 4
+    q, k, v, do = rnd((B, L, H, D), 30), rnd((B, L, Hkv, D), 31), rnd((B, L, Hkv, D), 32), rnd((B, L, H, D), 33)
+    dq, dk, dv, _ = orc.backward(q, k, v, do, causal)
+
+    def f(qq, kk, vv):
+        return float((orc.forward(qq, kk, vv, causal)[0] * do).sum())
+
+    eps = 1e-6
+    for name, x, g in (("q", q, dq), ("k", k, dk), ("v", v, dv)):
+        num = np.zeros_like(x)
+        for idx in np.ndindex(x.shape):
+            xp, xm = x.copy(), x.copy()
+            xp[idx] += eps
+            xm[idx] -= eps
+            args_p = {"q": q, "k": k, "v": v}
+            args_m = dict(args_p)
+            args_p[name], args_m[name] = xp, xm
+            num[idx] = (f(args_p["q"], args_p["k"], args_p["v"]) -
+                        f(args_m["q"], args_m["k"], args_m["v"])) / (2 * eps)
+        rel = np.abs(num - g).max() / max(1.0, np.abs(g).max())
+        assert rel < 1e-6, (name, rel)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_backward_column_sums(causal):
+    # sum_j dV_j = sum_i dO_i (rows of P sum to 1); sum_j dK_j = 0 (rows of dS sum to 0).
+    B, L, H, Hkv, D = 2, 31, 4, 2, 8
+    q, k, v, do = rnd((B, L, H, D), 34), rnd((B, L, Hkv, D), 35), rnd((B, L, Hkv, D), 36), rnd((B, L, H, D), 37)
+    _, dk, dv, _ = orc.backward(q, k, v, do, causal)
+    g = H // Hkv
+    do_sum = do.reshape(B, L, Hkv, g, D).sum(axis=(1, 3))
+    np.testing.assert_allclose(dv.sum(axis=1), do_sum, atol=1e-11)
+    np.testing.assert_allclose(dk.sum(axis=1), 0.0, atol=1e-11)
+
+
+def test_delta_is_rowwise_dot_product():
+    B, L, H, D = 2, 9, 3, 4
+    o, do = rnd((B, L, H, D), 38), rnd((B, L, H, D), 39)
+    got = orc.bwd_preprocess(o, do)
+    for b in range(B):
+        for h in range(H):
+            for i in range(L):
+                want = sum(o[b, i, h, d] * do[b, i, h, d] for d in range(D))
+                assert got[b, h, i] == pytest.approx(want, abs=1e-13)
+
+
+def test_backward_delta_uses_its_own_output():
+    B, L, H, D = 1, 12, 2, 8
+    q, k, v, do = rnd((B, L, H, D), 40), rnd((B, L, H, D), 41), rnd((B, L, H, D), 42), rnd((B, L, H, D), 43)
+    o, _ = orc.forward(q, k, v, True)
+    _, _, _, delta = orc.backward(q, k, v, do, True)
+    np.testing.assert_allclose(delta, orc.bwd_preprocess(o, do), atol=1e-13)
+
+
+def test_row_panels_do_not_change_results():
+    L, D = 70, 8
+    q, k, v, do = rnd((L, D), 44), rnd((L, D), 45), rnd((L, D), 46), rnd((L, D), 47)
+    for causal in (False, True):
+        a = orc.unit_backward(q, k, v, do, causal)
+        b = orc.unit_backward(q, k, v, do, causal, panel=16)
+        for x, y in zip(a, b):
+            np.testing.assert_allclose(x, y, atol=1e-13)
+        o1, l1 = orc.unit_forward(q, k, v, causal)
+        o2, l2 = orc.unit_forward(q, k, v, causal, panel=9)
+        np.testing.assert_allclose(o1, o2, atol=1e-14)
+        np.testing.assert_allclose(l1, l2, atol=1e-14)
+
+
+def test_sampled_rows_match_full_rows():
+    L, D = 50, 8
+    q, k, v = rnd((L, D), 48), rnd((L, D), 49), rnd((L, D), 50)
+    rows = np.array([0, 3, 17, 49])
+    for causal in (False, True):
+        o_full, l_full = orc.unit_forward(q, k, v, causal)
+        o_s, l_s = orc.unit_forward(q, k, v, causal, rows=rows)
+        np.testing.assert_allclose(o_s, o_full[rows], atol=1e-14)
+        np.testing.assert_allclose(l_s, l_full[rows], atol=1e-14)
+
+
+def test_inputs_are_seeded_and_rounded():
+    a = make_qkv(1, 8, 2, 1, 16, "fp16", seed=3)
+    b = make_qkv(1, 8, 2, 1, 16, "fp16", seed=3)
+    for x, y in zip(a, b):
+        assert torch.equal(x, y)
+    assert a[0].dtype == torch.float16 and a[1].shape == (1, 8, 1, 16)
+    c = make_qkv(1, 8, 2, 1, 16, "bf16", seed=3)
+    assert c[0].dtype == torch.bfloat16
+
+
+# ---------------------------------------------------------------- golden fixture
+
+def test_golden_config_small_fixture():
+    """Stored oracle values for the B1 H2 L128 D64 fp16 seed-0 case (written by
+    tests/golden/make_golden.py, which calls only the oracle)."""
+    import json
+    import os
+    path = os.path.join(os.path.dirname(__file__), "golden", "fwd_b1_h2_l128_d64_seed0.json")
+    with open(path) as fh:
+        gold = json.load(fh)
+    q, k, v, _ = make_qkv(1, 128, 2, 2, 64, "fp16", seed=0, with_do=False)
+    o, lse = orc.forward(q.double().numpy(), k.double().numpy(), v.double().numpy(), False)
+    for rec in gold["rows"]:
+        np.testing.assert_allclose(o[0, rec["i"], rec["h"]], rec["o"], atol=1e-12)
+        assert lse[0, rec["h"], rec["i"]] == pytest.approx(rec["lse"], abs=1e-12)
+
+
+# ---------------------------------------------------------------- pins have teeth
+
+def _mutant_forward(kind):
+    def fwd(q_bh, k_bh, v_bh, causal, rows=None, panel=4096):
+        L, D = q_bh.shape
+        scale = {"no_sqrt": 1.0 / D, "no_scale": 1.0}.get(kind, 1.0 / math.sqrt(D))
+        kk = k_bh
+        S = (q_bh @ kk.T) * scale
+        if kind == "transposed":
+            S = S.T
+        if causal:
+            mask = np.arange(L)[None, :] > np.arange(L)[:, None]
+            if kind == "mask_below":
+                mask = mask.T
+            if kind == "mask_inclusive":
+                mask = np.arange(L)[None, :] >= np.arange(L)[:, None]
+            S = np.where(mask, -np.inf, S)
+        m = S.max(axis=1, keepdims=True)
+        E = np.exp(S - m)
+        if kind == "colsum":
+            P = E / E.sum(axis=0, keepdims=True)
+        else:
+            P = E / E.sum(axis=1, keepdims=True)
+        lse = m[:, 0] + np.log(E.sum(axis=1))
+        if kind == "lse_no_max":
+            lse = np.log(E.sum(axis=1))
+        return P @ v_bh, lse
+    return fwd
+
+
+def _forward_pins(fwd):
+    """Run the forward pins against ``fwd``; return True when they all pass."""
+    try:
+        L, D = 12, 12
+        for causal in (False, True):
+            P, _ = fwd(rnd((L, D), 1), rnd((L, D), 2), np.eye(L), causal)
+            np.testing.assert_allclose(P.sum(axis=1), 1.0, atol=1e-12)
+            v = rnd((L, D), 6)
+            o, lse = fwd(np.zeros((L, D)), rnd((L, D), 7), v, causal)
+            want = (np.cumsum(v, axis=0) / np.arange(1, L + 1)[:, None]) if causal else np.tile(v.mean(0), (L, 1))
+            np.testing.assert_allclose(o, want, atol=1e-12)
+            want_lse = np.log(np.arange(1, L + 1)) if causal else np.full(L, math.log(L))
+            np.testing.assert_allclose(lse, want_lse, atol=1e-12)
+        B, L2, D2 = 1, 6, 3
+        q, k, v = rnd((B, L2, 1, D2), 19), rnd((B, L2, 1, D2), 20), rnd((B, L2, 1, D2), 21)
+        for causal in (False, True):
+            ob, lb = brute_force_forward(q, k, v, causal)
+            o, lse = fwd(q[0, :, 0], k[0, :, 0], v[0, :, 0], causal)
+            np.testing.assert_allclose(o, ob[0, :, 0], atol=1e-12)
+            np.testing.assert_allclose(lse, lb[0, 0], atol=1e-12)
+        return True
+    except AssertionError:
+        return False
+
+
+def test_planted_mistakes_are_caught():
+    assert _forward_pins(orc.unit_forward), "pins must pass on the oracle itself"
+    for kind in ("no_sqrt", "no_scale", "transposed", "mask_below", "mask_inclusive",
+                 "colsum", "lse_no_max"):
+        assert not _forward_pins(_mutant_forward(kind)), f"planted mistake {kind!r} not caught"
+
+
+def _mutant_backward(kind):
+    def bwd(q_bh, k_bh, v_bh, do_bh, causal, panel=4096):
+        L, D = q_bh.shape
+        inv = 1.0 / math.sqrt(D)
+        S = (q_bh @ k_bh.T) * inv
+        if causal:
+            S = np.where(np.arange(L)[None, :] > np.arange(L)[:, None], -np.inf, S)
+        m = S.max(axis=1, keepdims=True)
+        E = np.exp(S - m)
+        P = E / E.sum(axis=1, keepdims=True)
+        O = P @ v_bh
+        dl = (O * do_bh).sum(axis=1)
+        dv = (P @ do_bh) if kind == "dv_untransposed" else (P.T @ do_bh)
+        dP = do_bh @ v_bh.T
+        dS = P * dP if kind == "no_delta" else P * (dP - dl[:, None])
+        dq = dS @ k_bh * (1.0 if kind == "dq_unscaled" else inv)
+        dk = (dS @ q_bh if kind == "dk_untransposed" else dS.T @ q_bh) * inv
+        return dq, dk, dv
+    return bwd
+
+
+def _backward_pins(bwd):
+    try:
+        L, D = 5, 4
+        q, k, v, do = rnd((L, D), 60), rnd((L, D), 61), rnd((L, D), 62), rnd((L, D), 63)
+        for causal in (False, True):
+            dq, dk, dv = bwd(q, k, v, do, causal)[:3]
+            np.testing.assert_allclose(dv.sum(axis=0), do.sum(axis=0), atol=1e-11)
+            np.testing.assert_allclose(dk.sum(axis=0), 0.0, atol=1e-11)
+
+            def f(qq, kk, vv):
+                return float((orc.unit_forward(qq, kk, vv, causal)[0] * do).sum())
+            eps = 1e-6
+            for i, (x, g) in enumerate(((q, dq), (k, dk), (v, dv))):
+                num = np.zeros_like(x)
+                for idx in np.ndindex(x.shape):
+                    args_p, args_m = [q, k, v], [q, k, v]
+                    xp, xm = x.copy(), x.copy()
+                    xp[idx] += eps
+                    xm[idx] -= eps
+                    args_p[i], args_m[i] = xp, xm
+                    num[idx] = (f(*args_p) - f(*args_m)) / (2 * eps)
+                assert np.abs(num - g).max() / max(1.0, np.abs(g).max()) < 1e-6
+        return True
+    except AssertionError:
+        return False
+
+
+def test_planted_backward_mistakes_are_caught():
+    assert _backward_pins(orc.unit_backward), "pins must pass on the oracle itself"
+    for kind in ("dv_untransposed", "no_delta", "dq_unscaled", "dk_untransposed"):
+        assert not _backward_pins(_mutant_backward(kind)), f"planted mistake {kind!r} not caught"

@@ -1,0 +1,48 @@
+"""Seeded synthetic inputs shared by the tests, the benchmark and the oracle runs.
+
+This module holds no attention arithmetic: it only draws iid N(0, 1) values
+with a seeded CPU ``torch.Generator`` and rounds them to the storage dtype, so
+the CUDA path and the CPU oracle see the same bytes.
+
+Recipe (the pages benchmark on random tensors of the attention shapes, with no
+dataset): Q [B, L, H, D], then K and V [B, L, Hkv, D], then dO [B, L, H, D],
+drawn in that order from one generator seeded with ``seed``, in float32, then
+cast with round-to-nearest-even to fp16 or bf16.
+"""
+
+from __future__ import annotations
+
+import torch
+
+_DTYPES = {"fp16": torch.float16, "bf16": torch.bfloat16,
+           "f16": torch.float16, torch.float16: torch.float16,
+           torch.bfloat16: torch.bfloat16}
+
+
+def storage_dtype(dt) -> torch.dtype:
+    """Map 'fp16' / 'bf16' (or a torch dtype) to the torch storage dtype."""
+    try:
+        return _DTYPES[dt]
+    except KeyError as e:
+        raise ValueError(f"unsupported dtype {dt!r}: use fp16 or bf16") from e
+
+
+def make_qkv(B: int, L: int, H: int, Hkv: int, D: int, dtype="fp16",
+             seed: int = 0, with_do: bool = True):
+    """Return (q, k, v, do) CPU tensors; do is None when ``with_do`` is False."""
+    g = torch.Generator(device="cpu")
+    g.manual_seed(int(seed))
+    dt = storage_dtype(dtype)
+    q = torch.randn(B, L, H, D, generator=g, dtype=torch.float32).to(dt)
+    k = torch.randn(B, L, Hkv, D, generator=g, dtype=torch.float32).to(dt)
+    v = torch.randn(B, L, Hkv, D, generator=g, dtype=torch.float32).to(dt)
+    do = None
+    if with_do:
+        do = torch.randn(B, L, H, D, generator=g, dtype=torch.float32).to(dt)
+    return q, k, v, do
+
+
+def make_unit(L: int, D: int, dtype="fp16", seed: int = 0, group: int = 1):
+    """One (batch, kv-head) unit with ``group`` query heads: shapes [1, L, group, D]
+    for Q/dO and [1, L, 1, D] for K/V.  Used for small, fast cases."""
+    return make_qkv(1, L, group, 1, D, dtype, seed)
