@@ -1,0 +1,115 @@
+/*
+ * C ABI of the GB300 (sm_103a) tiled online-softmax attention library.
+ *
+ * Tensors are plain device pointers; sizes are ints; nothing here depends on
+ * a framework.  Every call is asynchronous on the given CUDA stream (passed as
+ * `void*`, i.e. a cudaStream_t; NULL = the legacy default stream).  Argument
+ * errors are reported synchronously by the return value and launch nothing.
+ * The caller allocates and owns every buffer, including the backward
+ * workspace; the library keeps only a per-device SM-count cache.
+ *
+ * Layouts (all contiguous, row-major):
+ *   Q, O, dO, dQ   [B, L, H,   D]   fp16 or bf16 ("BSHD")
+ *   K, V, dK, dV   [B, L, Hkv, D]   same dtype as Q
+ *   LSE, Delta     [B, H, L]        fp32
+ * Query head h reads K/V head h / (H / Hkv) (grouped-query attention).
+ * The softmax scale is fixed at 1 / sqrt(D).  Causal masking is top-left
+ * aligned with one length L for queries and keys: key j is visible to query i
+ * iff j <= i.  Every pointer must be 16-byte aligned.
+ * Supported: D in {64, 128}; L >= 1; B, H, Hkv >= 1 with H % Hkv == 0;
+ * B * H * L and B * L * H * D must fit the kernels' 32-bit coordinates
+ * (B, L, H < 2^31 and B * L * H * D < 2^40).
+ */
+#ifndef TILED_ATTENTION_FA_GB300_FA_H
+#define TILED_ATTENTION_FA_GB300_FA_H
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  FA_OK = 0,
+  FA_ERR_INVALID_ARG = 1,    /* null/misaligned pointer, bad size, H % Hkv != 0 */
+  FA_ERR_UNSUPPORTED = 2,    /* D or dtype outside the supported set */
+  FA_ERR_CUDA = 3,           /* a CUDA runtime call or kernel launch failed */
+  FA_ERR_DEVICE_TIMEOUT = 4  /* a kernel gave up a bounded wait (see fa_check_device_error) */
+} fa_status;
+
+typedef enum { FA_F16 = 0, FA_BF16 = 1 } fa_dtype;
+
+/*
+ * Forward attention.  For each batch b and query head h:
+ *   S = Q_bh K_bh'^T / sqrt(D)   (h' = h / (H / Hkv)), causal: S_ij = -inf for j > i
+ *   O_bh = softmax_rows(S) V_bh'                 -> O   [B, L, H, D]
+ *   LSE_bh,i = ln sum_j exp(S_ij)                -> LSE [B, H, L], fp32
+ * Page "使用 TileLang 在 AMD GPU 上快速开发高性能 Flash Attention", sections
+ * 核心公式与计算流程 (the formulas) and K/V Tile 遍历与核心计算 (the tiled
+ * online-softmax loop this kernel implements); the LSE is the per-row
+ * statistic the backward kernel of page "TileLang与机器学习训练：反向传播算子优化案例"
+ * takes as input (section 算子拆分与流水线设计).
+ * Q, K, V are read only.  O and LSE are written in full (LSE may not be NULL).
+ */
+fa_status fa_fwd(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int L,
+                 int H, int Hkv, int D, int causal, int dtype, void* stream);
+
+/*
+ * Backward preprocess: Delta[b, h, i] = sum_d O[b, i, h, d] * dO[b, i, h, d]
+ * (fp32 accumulation), the per-row term of the softmax gradient.  Page
+ * "TileLang与机器学习训练：反向传播算子优化案例", section 算子拆分与流水线设计
+ * (the "Delta" preprocessing stage; its printed block product is read as this
+ * per-row dot product).  When `dq_accum` is not NULL it must point to
+ * fa_bwd_workspace_size(B, L, H, D) bytes, which this call sets to zero in
+ * the same pass, ready for fa_bwd.
+ */
+fa_status fa_bwd_preprocess(const void* O, const void* dO, float* Delta, float* dq_accum, int B,
+                            int L, int H, int D, int dtype, void* stream);
+
+/* Bytes of the fp32 dQ accumulator fa_bwd needs: B * H * ceil(L/128)*128 * D * 4. */
+size_t fa_bwd_workspace_size(int B, int L, int H, int D);
+
+/*
+ * Backward attention: dQ, dK, dV of the forward above, given dO, the forward's
+ * LSE and fa_bwd_preprocess's Delta.  With P = exp(S - LSE):
+ *   dV = P^T dO,  dP = dO V^T,  dS = P o (dP - Delta),
+ *   dQ = dS K / sqrt(D),  dK = dS^T Q / sqrt(D),
+ * with dK, dV of a K/V head summed over its query heads.  Page
+ * "TileLang与机器学习训练：反向传播算子优化案例", sections 算子拆分与流水线设计
+ * (one K/V tile per CTA looping over Q tiles, dV accumulated from the
+ * transposed probabilities) and 内存布局优化 (dQ accumulated in fp32 through
+ * atomics into a layout matched to the accumulator fragments, then a
+ * post-processing pass).
+ * `dq_accum` is the caller's workspace (fa_bwd_workspace_size bytes, 16-byte
+ * aligned); it must hold zeros on entry unless `zero_accum` is non-zero, in
+ * which case this call zeroes it first.  Its contents afterwards are
+ * unspecified.  O is accepted for interface symmetry and is not read (Delta
+ * carries it); it may be NULL.  dQ, dK, dV are written in full.
+ */
+fa_status fa_bwd(const void* Q, const void* K, const void* V, const void* O, const void* dO,
+                 const float* LSE, const float* Delta, void* dQ, void* dK, void* dV,
+                 float* dq_accum, int zero_accum, int B, int L, int H, int Hkv, int D, int causal,
+                 int dtype, void* stream);
+
+/*
+ * Synchronise `stream` and report whether any kernel of this library gave up
+ * a bounded wait since the last check (FA_ERR_DEVICE_TIMEOUT; the word is then
+ * cleared).  Kernels never trap or spin forever: a wait that exceeds about one
+ * second records its site id, unwinds the CTA and returns.
+ */
+fa_status fa_check_device_error(void* stream);
+
+/* Site id recorded by the last FA_ERR_DEVICE_TIMEOUT (0 if none). */
+unsigned int fa_last_error_site(void);
+
+/* Static, human-readable text for a status value. */
+const char* fa_status_string(fa_status status);
+
+/* Library version string. */
+const char* fa_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TILED_ATTENTION_FA_GB300_FA_H */

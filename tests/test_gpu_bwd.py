@@ -1,0 +1,80 @@
+"""Backward parity: preprocess (Delta) and dQ/dK/dV against the fp64 oracle.
+
+The GPU backward consumes the GPU forward's O and LSE; the oracle recomputes
+its own from the same inputs."""
+
+import numpy as np
+import pytest
+import torch
+
+import tiled_attention_fa_gb300 as fa
+from tests.helpers import assert_close, inputs, to64
+from oracle import fa_oracle as orc
+
+pytestmark = pytest.mark.gpu
+
+
+def gpu_fwd_bwd(qd, kd, vd, dod, causal):
+    o, lse = fa.fwd(qd, kd, vd, causal)
+    dq, dk, dv, delta = fa.attention_backward(qd, kd, vd, o, lse, dod, causal)
+    torch.cuda.synchronize()
+    fa.check_device_error()
+    return o, lse, dq, dk, dv, delta
+
+
+def run_and_compare(B, L, H, Hkv, D, dtype, causal, seed):
+    (q, k, v, do), (qd, kd, vd, dod) = inputs(B, L, H, Hkv, D, dtype, seed)
+    o, lse, dq, dk, dv, delta = gpu_fwd_bwd(qd, kd, vd, dod, causal)
+    rq, rk, rv, rdelta = orc.backward(q, k, v, do, causal)
+    assert_close(to64(dv), rv, name="dV")
+    assert_close(to64(dk), rk, name="dK")
+    assert_close(to64(dq), rq, name="dQ")
+    # Delta of the GPU's own O against the oracle's Delta (diagnostic bound).
+    d = to64(delta)
+    assert np.all(np.abs(d - rdelta) <= 1e-2 * np.maximum(1.0, np.abs(rdelta))), "Delta"
+
+
+def test_preprocess_matches_definition(cuda_lib):
+    for (B, L, H, D, dt) in [(2, 77, 3, 64, "fp16"), (1, 300, 4, 128, "bf16"), (3, 1, 2, 128, "fp16")]:
+        g = torch.Generator().manual_seed(L)
+        dtt = torch.float16 if dt == "fp16" else torch.bfloat16
+        o = torch.randn(B, L, H, D, generator=g).to(dtt)
+        do = torch.randn(B, L, H, D, generator=g).to(dtt)
+        acc = torch.full((fa.workspace_size(B, L, H, D) // 4,), 7.0, device="cuda")
+        delta = fa.bwd_preprocess(o.cuda(), do.cuda(), dq_accum=acc)
+        torch.cuda.synchronize()
+        ref = orc.bwd_preprocess(to64(o), to64(do))
+        assert_close(to64(delta), ref, rtol=1e-5, atol=1e-4, name="Delta")
+        assert torch.count_nonzero(acc).item() == 0, "accumulator not zeroed"
+
+
+def test_smallest_case(cuda_lib):
+    run_and_compare(1, 128, 2, 2, 64, "fp16", False, 0)
+
+
+@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("L", [1, 17, 127, 128, 129, 255, 256, 300, 513])
+def test_ragged_lengths(cuda_lib, L, causal, D):
+    run_and_compare(1, L, 2, 2, D, "fp16", causal, seed=100 + L)
+
+
+@pytest.mark.parametrize("H,Hkv", [(1, 1), (4, 1), (8, 2)])
+@pytest.mark.parametrize("dtype", ["fp16", "bf16"])
+@pytest.mark.parametrize("causal", [False, True])
+def test_heads_and_dtypes(cuda_lib, H, Hkv, dtype, causal):
+    run_and_compare(2, 384, H, Hkv, 128, dtype, causal, seed=H * 10 + Hkv)
+    run_and_compare(2, 320, H, Hkv, 64, dtype, causal, seed=H * 10 + Hkv + 1)
+
+
+def test_unzeroed_accumulator_path(cuda_lib):
+    """fa_bwd zeroes a dirty workspace itself when told it is not zeroed."""
+    (q, k, v, do), (qd, kd, vd, dod) = inputs(1, 256, 2, 1, 64, "fp16", 3)
+    o, lse = fa.fwd(qd, kd, vd, True)
+    delta = fa.bwd_preprocess(o, dod)
+    acc = torch.full((fa.workspace_size(1, 256, 2, 64) // 4,), 3.0, device="cuda")
+    dq, dk, dv = fa.bwd(qd, kd, vd, o, dod, lse, delta, True, dq_accum=acc, accum_zeroed=False)
+    rq, rk, rv, _ = orc.backward(q, k, v, do, True)
+    assert_close(to64(dq), rq, name="dQ")
+    assert_close(to64(dk), rk, name="dK")
+    assert_close(to64(dv), rv, name="dV")

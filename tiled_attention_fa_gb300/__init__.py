@@ -1,0 +1,21 @@
+"""GB300-native (sm_103a) tiled online-softmax attention, forward and backward.
+
+The compute path is the C-ABI library ``libfa_gb300.so`` (hand-written CUDA:
+TMA, tcgen05 MMA with TMEM accumulators, warp-specialised pipelines); this
+package only marshals torch tensors into it.  Build the library with
+``python -m tiled_attention_fa_gb300.build``.
+"""
+
+from .api import (  # noqa: F401
+    HostRunner,
+    alloc_workspace,
+    attention_backward,
+    bwd,
+    bwd_preprocess,
+    check_device_error,
+    fwd,
+    workspace_size,
+)
+
+__all__ = ["fwd", "bwd_preprocess", "bwd", "attention_backward", "workspace_size",
+           "alloc_workspace", "check_device_error", "HostRunner"]

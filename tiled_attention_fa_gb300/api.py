@@ -1,0 +1,193 @@
+"""Python binding of the C ABI: argument marshalling only.
+
+Every function takes torch CUDA tensors (PyTorch supplies device memory and
+the current stream), checks layout and dtype, and calls the matching C entry
+point.  All arithmetic runs in the library's CUDA kernels; there is no CPU or
+framework fallback.  ``HostRunner`` serves callers whose data lives on the
+host: it copies through pinned host memory around the same calls.
+"""
+
+from __future__ import annotations
+
+import torch
+
+from . import _lib
+
+_DT = {torch.float16: _lib.FA_F16, torch.bfloat16: _lib.FA_BF16}
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    try:
+        return _DT[t.dtype]
+    except KeyError as e:
+        raise TypeError(f"dtype {t.dtype} unsupported: use float16 or bfloat16") from e
+
+
+def _need(t: torch.Tensor, name: str, shape=None, dtype=None):
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name} has dtype {t.dtype}, expected {dtype}")
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def fwd(q, k, v, causal: bool = False, out=None, lse=None, stream=None):
+    """O, LSE = attention(Q, K, V).  q [B, L, H, D]; k, v [B, L, Hkv, D]."""
+    B, L, H, D = q.shape
+    Hkv = k.shape[2]
+    _need(q, "q")
+    _need(k, "k", (B, L, Hkv, D), q.dtype)
+    _need(v, "v", (B, L, Hkv, D), q.dtype)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty(B, H, L, device=q.device, dtype=torch.float32)
+    _need(out, "out", q.shape, q.dtype)
+    _need(lse, "lse", (B, H, L), torch.float32)
+    lib = _lib.load()
+    st = lib.fa_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
+                    B, L, H, Hkv, D, int(bool(causal)), _dtype_code(q), _stream(stream))
+    _lib.check("fa_fwd", st)
+    return out, lse
+
+
+def workspace_size(B: int, L: int, H: int, D: int) -> int:
+    """Bytes of the fp32 dQ accumulator the backward needs."""
+    return int(_lib.load().fa_bwd_workspace_size(B, L, H, D))
+
+
+def alloc_workspace(B: int, L: int, H: int, D: int, device) -> torch.Tensor:
+    n = workspace_size(B, L, H, D) // 4
+    return torch.empty(n, device=device, dtype=torch.float32)
+
+
+def bwd_preprocess(o, do, delta=None, dq_accum=None, stream=None):
+    """Delta[b, h, i] = sum_d O[b, i, h, d] dO[b, i, h, d]; optionally zero dq_accum."""
+    B, L, H, D = o.shape
+    _need(o, "o")
+    _need(do, "do", o.shape, o.dtype)
+    if delta is None:
+        delta = torch.empty(B, H, L, device=o.device, dtype=torch.float32)
+    _need(delta, "delta", (B, H, L), torch.float32)
+    acc_ptr = 0
+    if dq_accum is not None:
+        _need(dq_accum, "dq_accum", dtype=torch.float32)
+        if dq_accum.numel() * 4 < workspace_size(B, L, H, D):
+            raise ValueError("dq_accum is smaller than workspace_size()")
+        acc_ptr = dq_accum.data_ptr()
+    st = _lib.load().fa_bwd_preprocess(o.data_ptr(), do.data_ptr(), delta.data_ptr(), acc_ptr or None,
+                                       B, L, H, D, _dtype_code(o), _stream(stream))
+    _lib.check("fa_bwd_preprocess", st)
+    return delta
+
+
+def bwd(q, k, v, o, do, lse, delta, causal: bool = False, dq=None, dk=None, dv=None,
+        dq_accum=None, accum_zeroed: bool = False, stream=None):
+    """dQ, dK, dV of the forward.  ``dq_accum`` is the fp32 workspace; unless
+    ``accum_zeroed`` (fa_bwd_preprocess zeroed it) the call zeroes it first."""
+    B, L, H, D = q.shape
+    Hkv = k.shape[2]
+    _need(q, "q")
+    for name, t, shp in (("k", k, (B, L, Hkv, D)), ("v", v, (B, L, Hkv, D)), ("do", do, q.shape)):
+        _need(t, name, shp, q.dtype)
+    _need(lse, "lse", (B, H, L), torch.float32)
+    _need(delta, "delta", (B, H, L), torch.float32)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    _need(dq, "dq", q.shape, q.dtype)
+    _need(dk, "dk", k.shape, q.dtype)
+    _need(dv, "dv", v.shape, q.dtype)
+    if dq_accum is None:
+        dq_accum = alloc_workspace(B, L, H, D, q.device)
+        accum_zeroed = False
+    _need(dq_accum, "dq_accum", dtype=torch.float32)
+    if dq_accum.numel() * 4 < workspace_size(B, L, H, D):
+        raise ValueError("dq_accum is smaller than workspace_size()")
+    st = _lib.load().fa_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(),
+                            o.data_ptr() if o is not None else None, do.data_ptr(),
+                            lse.data_ptr(), delta.data_ptr(), dq.data_ptr(), dk.data_ptr(),
+                            dv.data_ptr(), dq_accum.data_ptr(), 0 if accum_zeroed else 1,
+                            B, L, H, Hkv, D, int(bool(causal)), _dtype_code(q), _stream(stream))
+    _lib.check("fa_bwd", st)
+    return dq, dk, dv
+
+
+def attention_backward(q, k, v, o, lse, do, causal: bool = False, dq_accum=None, stream=None):
+    """Preprocess + backward in one call (Delta computed here, accumulator zeroed in the same pass)."""
+    B, L, H, D = q.shape
+    if dq_accum is None:
+        dq_accum = alloc_workspace(B, L, H, D, q.device)
+    delta = bwd_preprocess(o, do, dq_accum=dq_accum, stream=stream)
+    dq, dk, dv = bwd(q, k, v, o, do, lse, delta, causal, dq_accum=dq_accum, accum_zeroed=True,
+                     stream=stream)
+    return dq, dk, dv, delta
+
+
+def check_device_error(stream=None) -> None:
+    """Synchronise and raise if a kernel gave up a bounded wait since the last check."""
+    lib = _lib.load()
+    st = lib.fa_check_device_error(_stream(stream))
+    if st != _lib.FA_OK:
+        raise _lib.FAError(f"device (site {lib.fa_last_error_site()})", st)
+
+
+class HostRunner:
+    """Forward + backward for host-resident tensors through pinned buffers.
+
+    ``run(q, k, v, do)`` copies the CPU inputs to the device, runs the
+    forward, the preprocess and the backward, and copies O, LSE, dQ, dK, dV
+    back into pinned host tensors (returned).  Device buffers are allocated
+    once per shape and reused.
+    """
+
+    def __init__(self, B, L, H, Hkv, D, dtype=torch.float16, causal=False, device="cuda"):
+        self.causal = causal
+        dev = torch.device(device)
+        self.q = torch.empty(B, L, H, D, dtype=dtype, device=dev)
+        self.k = torch.empty(B, L, Hkv, D, dtype=dtype, device=dev)
+        self.v = torch.empty_like(self.k)
+        self.do = torch.empty_like(self.q)
+        self.o = torch.empty_like(self.q)
+        self.lse = torch.empty(B, H, L, dtype=torch.float32, device=dev)
+        self.delta = torch.empty_like(self.lse)
+        self.dq = torch.empty_like(self.q)
+        self.dk = torch.empty_like(self.k)
+        self.dv = torch.empty_like(self.k)
+        self.acc = alloc_workspace(B, L, H, D, dev)
+        pin = dict(pin_memory=True)
+        self.h_out = {
+            "o": torch.empty(self.o.shape, dtype=dtype, **pin),
+            "lse": torch.empty(self.lse.shape, dtype=torch.float32, **pin),
+            "dq": torch.empty(self.dq.shape, dtype=dtype, **pin),
+            "dk": torch.empty(self.dk.shape, dtype=dtype, **pin),
+            "dv": torch.empty(self.dv.shape, dtype=dtype, **pin),
+        }
+
+    def h2d_bytes(self) -> int:
+        return sum(t.numel() * t.element_size() for t in (self.q, self.k, self.v, self.do))
+
+    def d2h_bytes(self) -> int:
+        return sum(t.numel() * t.element_size() for t in self.h_out.values())
+
+    def run(self, q, k, v, do, stream=None):
+        for dst, src in ((self.q, q), (self.k, k), (self.v, v), (self.do, do)):
+            dst.copy_(src, non_blocking=True)
+        fwd(self.q, self.k, self.v, self.causal, out=self.o, lse=self.lse, stream=stream)
+        bwd_preprocess(self.o, self.do, delta=self.delta, dq_accum=self.acc, stream=stream)
+        bwd(self.q, self.k, self.v, self.o, self.do, self.lse, self.delta, self.causal,
+            dq=self.dq, dk=self.dk, dv=self.dv, dq_accum=self.acc, accum_zeroed=True,
+            stream=stream)
+        for name, src in (("o", self.o), ("lse", self.lse), ("dq", self.dq), ("dk", self.dk),
+                          ("dv", self.dv)):
+            self.h_out[name].copy_(src, non_blocking=True)
+        return self.h_out

@@ -1,0 +1,99 @@
+// C ABI: argument validation and dispatch to the kernel units.
+#include <cstdint>
+
+#include "../../include/fa.h"
+#include "internal.h"
+
+namespace {
+
+unsigned int g_last_site = 0;
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool ptr_ok(const void* p) { return p != nullptr && aligned16(p); }
+
+fa_status check_shape(int B, int L, int H, int Hkv, int D, int dtype) {
+  if (B < 1 || L < 1 || H < 1 || Hkv < 1) return FA_ERR_INVALID_ARG;
+  if (L > (1 << 30) || H > (1 << 20) || B > (1 << 20)) return FA_ERR_INVALID_ARG;
+  if (H % Hkv != 0) return FA_ERR_INVALID_ARG;
+  if (dtype != FA_F16 && dtype != FA_BF16) return FA_ERR_UNSUPPORTED;
+  if (D != 64 && D != 128) return FA_ERR_UNSUPPORTED;
+  // Work-item and element counts must fit the kernels' integer arithmetic.
+  const long long items = static_cast<long long>(B) * H * ((L + 255) / 256);
+  const long long elems = static_cast<long long>(B) * fa::padded_len(L) * H * D;
+  if (items >= (1ll << 31) || elems >= (1ll << 40)) return FA_ERR_INVALID_ARG;
+  if (static_cast<long long>(B) * H * fa::padded_len(L) >= (1ll << 31)) return FA_ERR_INVALID_ARG;
+  return FA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+fa_status fa_fwd(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int L,
+                 int H, int Hkv, int D, int causal, int dtype, void* stream) {
+  fa_status st = check_shape(B, L, H, Hkv, D, dtype);
+  if (st != FA_OK) return st;
+  if (!ptr_ok(Q) || !ptr_ok(K) || !ptr_ok(V) || !ptr_ok(O) || !ptr_ok(LSE))
+    return FA_ERR_INVALID_ARG;
+  return fa::run_fwd(Q, K, V, O, LSE, B, L, H, Hkv, D, causal, dtype,
+                     static_cast<cudaStream_t>(stream));
+}
+
+fa_status fa_bwd_preprocess(const void* O, const void* dO, float* Delta, float* dq_accum, int B,
+                            int L, int H, int D, int dtype, void* stream) {
+  fa_status st = check_shape(B, L, H, H, D, dtype);
+  if (st != FA_OK) return st;
+  if (!ptr_ok(O) || !ptr_ok(dO) || !ptr_ok(Delta)) return FA_ERR_INVALID_ARG;
+  if (dq_accum != nullptr && !aligned16(dq_accum)) return FA_ERR_INVALID_ARG;
+  return fa::run_bwd_prep(O, dO, Delta, dq_accum, B, L, H, D, dtype,
+                          static_cast<cudaStream_t>(stream));
+}
+
+size_t fa_bwd_workspace_size(int B, int L, int H, int D) {
+  if (B < 1 || L < 1 || H < 1 || D < 1) return 0;
+  return static_cast<size_t>(B) * H * fa::padded_len(L) * D * sizeof(float);
+}
+
+fa_status fa_bwd(const void* Q, const void* K, const void* V, const void* O, const void* dO,
+                 const float* LSE, const float* Delta, void* dQ, void* dK, void* dV,
+                 float* dq_accum, int zero_accum, int B, int L, int H, int Hkv, int D, int causal,
+                 int dtype, void* stream) {
+  (void)O;
+  fa_status st = check_shape(B, L, H, Hkv, D, dtype);
+  if (st != FA_OK) return st;
+  if (!ptr_ok(Q) || !ptr_ok(K) || !ptr_ok(V) || !ptr_ok(dO) || !ptr_ok(LSE) || !ptr_ok(Delta) ||
+      !ptr_ok(dQ) || !ptr_ok(dK) || !ptr_ok(dV) || !ptr_ok(dq_accum))
+    return FA_ERR_INVALID_ARG;
+  return fa::run_bwd(Q, K, V, dO, LSE, Delta, dQ, dK, dV, dq_accum, zero_accum, B, L, H, Hkv, D,
+                     causal, dtype, static_cast<cudaStream_t>(stream));
+}
+
+fa_status fa_check_device_error(void* stream) {
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const unsigned int a = fa::fwd_read_error(s);
+  const unsigned int b = fa::bwd_read_error(s);
+  if (a == 0xFFFFFFFFu || b == 0xFFFFFFFFu) return FA_ERR_CUDA;
+  if (a || b) {
+    g_last_site = a ? a : b;
+    return FA_ERR_DEVICE_TIMEOUT;
+  }
+  return FA_OK;
+}
+
+unsigned int fa_last_error_site(void) { return g_last_site; }
+
+const char* fa_status_string(fa_status s) {
+  switch (s) {
+    case FA_OK: return "ok";
+    case FA_ERR_INVALID_ARG: return "invalid argument";
+    case FA_ERR_UNSUPPORTED: return "unsupported head dimension or dtype";
+    case FA_ERR_CUDA: return "CUDA runtime or launch error";
+    case FA_ERR_DEVICE_TIMEOUT: return "a kernel gave up a bounded wait";
+  }
+  return "unknown status";
+}
+
+const char* fa_version(void) { return "tiled_attention_fa_gb300 0.1 (sm_103a)"; }
+
+}  // extern "C"

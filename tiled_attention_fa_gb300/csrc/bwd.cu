@@ -1,0 +1,100 @@
+// Host launchers of the backward kernels (preprocess, main pass, dQ post-process).
+#include <type_traits>
+
+#include "bwd.cuh"
+#include "common.cuh"
+#include "internal.h"
+
+namespace fa {
+
+template <int D, bool BF16>
+static fa_status launch_prep(const void* O, const void* dO, float* Delta, float* dq_accum, int B,
+                             int L, int H, cudaStream_t s) {
+  const int Lpad = padded_len(L);
+  const int grid = B * (Lpad / 32);
+  const size_t smem = static_cast<size_t>(H) * 32 * sizeof(float);
+  auto kern = fa_bwd_prep_kernel<D, BF16>;
+  if (smem > 48 * 1024 &&
+      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+          cudaSuccess)
+    return FA_ERR_UNSUPPORTED;
+  kern<<<grid, 256, smem, s>>>(O, dO, Delta, dq_accum, B, L, H, Lpad);
+  return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+fa_status run_bwd_prep(const void* O, const void* dO, float* Delta, float* dq_accum, int B, int L,
+                       int H, int D, int dtype, cudaStream_t s) {
+  const bool bf16 = dtype == FA_BF16;
+  if (static_cast<size_t>(H) * 32 * sizeof(float) > 200 * 1024) return FA_ERR_UNSUPPORTED;
+  if (D == 64)
+    return bf16 ? launch_prep<64, true>(O, dO, Delta, dq_accum, B, L, H, s)
+                : launch_prep<64, false>(O, dO, Delta, dq_accum, B, L, H, s);
+  return bf16 ? launch_prep<128, true>(O, dO, Delta, dq_accum, B, L, H, s)
+              : launch_prep<128, false>(O, dO, Delta, dq_accum, B, L, H, s);
+}
+
+template <int D, bool BF16>
+static fa_status launch_bwd(const void* Q, const void* K, const void* V, const void* dO,
+                            const float* LSE, const float* Delta, void* dQ, void* dK, void* dV,
+                            float* dq_accum, int zero_accum, int B, int L, int H, int Hkv,
+                            int causal, cudaStream_t s) {
+  using Ly = BwdLayout<D>;
+  const int Lpad = padded_len(L);
+  if (zero_accum &&
+      cudaMemsetAsync(dq_accum, 0, static_cast<size_t>(B) * H * Lpad * D * sizeof(float), s) !=
+          cudaSuccess)
+    return FA_ERR_CUDA;
+  CUtensorMap tq, tk, tv, tdo;
+  if (!make_bshd_map(&tq, Q, B, L, H, D, BF16) || !make_bshd_map(&tk, K, B, L, Hkv, D, BF16) ||
+      !make_bshd_map(&tv, V, B, L, Hkv, D, BF16) || !make_bshd_map(&tdo, dO, B, L, H, D, BF16))
+    return FA_ERR_CUDA;
+  BwdParams p;
+  p.LSE = LSE;
+  p.Delta = Delta;
+  p.dq_accum = dq_accum;
+  p.dK = dK;
+  p.dV = dV;
+  p.B = B;
+  p.L = L;
+  p.H = H;
+  p.Hkv = Hkv;
+  p.causal = causal ? 1 : 0;
+  p.n_kv = Lpad / 128;
+  p.Lpad = Lpad;
+  p.n_items = B * Hkv * p.n_kv;
+  p.scale = 1.f / sqrtf(static_cast<float>(D));
+  p.sl2 = 1.4426950408889634f * p.scale;
+  int dev = 0, optin = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+  if (optin < static_cast<int>(Ly::SMEM_ALLOC)) return FA_ERR_UNSUPPORTED;
+  auto kern = fa_bwd_kernel<D, BF16>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Ly::SMEM_ALLOC) !=
+      cudaSuccess)
+    return FA_ERR_CUDA;
+  kern<<<p.n_items, Ly::NTHREADS, Ly::SMEM_ALLOC, s>>>(tq, tk, tv, tdo, p);
+  if (cudaGetLastError() != cudaSuccess) return FA_ERR_CUDA;
+  fa_dq_convert_kernel<D, BF16><<<B * H * (Lpad / 64), 256, 0, s>>>(dq_accum, dQ, B, L, H, Lpad,
+                                                                    p.scale);
+  return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+fa_status run_bwd(const void* Q, const void* K, const void* V, const void* dO, const float* LSE,
+                  const float* Delta, void* dQ, void* dK, void* dV, float* dq_accum,
+                  int zero_accum, int B, int L, int H, int Hkv, int D, int causal, int dtype,
+                  cudaStream_t s) {
+  const bool bf16 = dtype == FA_BF16;
+  if (D == 64)
+    return bf16 ? launch_bwd<64, true>(Q, K, V, dO, LSE, Delta, dQ, dK, dV, dq_accum, zero_accum,
+                                       B, L, H, Hkv, causal, s)
+                : launch_bwd<64, false>(Q, K, V, dO, LSE, Delta, dQ, dK, dV, dq_accum, zero_accum,
+                                        B, L, H, Hkv, causal, s);
+  return bf16 ? launch_bwd<128, true>(Q, K, V, dO, LSE, Delta, dQ, dK, dV, dq_accum, zero_accum, B,
+                                      L, H, Hkv, causal, s)
+              : launch_bwd<128, false>(Q, K, V, dO, LSE, Delta, dQ, dK, dV, dq_accum, zero_accum,
+                                       B, L, H, Hkv, causal, s);
+}
+
+unsigned int bwd_read_error(cudaStream_t s) { return read_and_clear_error(s); }
+
+}  // namespace fa

@@ -1,0 +1,520 @@
+// Backward attention kernels for sm_103a.
+//
+// Method (page "TileLang与机器学习训练：反向传播算子优化案例", sections
+// 算子拆分与流水线设计 and 内存布局优化): three stages --
+//   1. preprocess: Delta_i = sum_d O_id dO_id per query row;
+//   2. main pass: one CTA per K/V tile that loops over the Q tiles,
+//      recomputes the transposed scores, accumulates dV from the transposed
+//      probabilities (and, completing the elided steps with the analytic
+//      gradient, dK from dS^T Q), and adds each dQ partial into an fp32
+//      accumulator with atomics laid out to match the accumulator fragments;
+//   3. post-process: scale and convert the dQ accumulator back to BSHD.
+//
+// GB300 design of the main pass (320 threads, one CTA per SM, one K/V tile per CTA):
+//   warps 0-3  "softmax" warpgroup: thread r owns key row r of the K/V tile;
+//              P^T = exp2(S^T*c - LSE*log2e), dS^T = P^T o (dP^T - Delta);
+//              P^T goes to TMEM (A operand of dV += P^T dO), dS^T to swizzled
+//              smem (A operand of dK += dS^T Q and, read MN-major, of
+//              dQ = dS K); at the end it writes dK.
+//   warps 4-7  dQ drain: thread r owns query row r; reads the dQ tile from
+//              TMEM and adds it into the fp32 accumulator with 16-byte vector
+//              atomics; at the end it writes dV.
+//   warp  8    TMA producer: K_j, V_j once; then Q_i, dO_i (and LSE_i,
+//              Delta_i) through a two-slot ring.
+//   warp  9    TMEM allocator and the single tcgen05.mma issuing thread.
+// dK and dV stay in TMEM for the whole CTA; for grouped-query attention the
+// CTA loops over every query head of its K/V head, so dK/dV need no atomics.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "common.cuh"
+#include "fwd.cuh"  // pack2
+#include "ptx.cuh"
+
+namespace fa {
+
+struct BwdParams {
+  const float* LSE;    // [B, H, L]
+  const float* Delta;  // [B, H, L]
+  float* dq_accum;     // [B, H, D/4, Lpad, 4]
+  void* dK;            // [B, L, Hkv, D]
+  void* dV;            // [B, L, Hkv, D]
+  int B, L, H, Hkv, causal;
+  int n_kv;     // ceil(L / 128) (also the number of Q tiles)
+  int Lpad;     // n_kv * 128
+  int n_items;  // B * Hkv * n_kv
+  float sl2;    // log2(e) / sqrt(D)
+  float scale;  // 1 / sqrt(D)
+};
+
+template <int D>
+struct BwdLayout {
+  static constexpr int KCH = D / 64;
+  static constexpr uint32_t CHUNK = 128u * 128u;
+  static constexpr uint32_t TILE = KCH * CHUNK;
+  static constexpr int STAGES = 2;
+  // Small region first (barriers, TMEM address, abort flag, LSE/Delta slots),
+  // then the 1024-byte aligned operand tiles.
+  static constexpr int B_KVFULL = 0, B_QFULL = 1, B_QEMPTY = 1 + STAGES, B_SFULL = 1 + 2 * STAGES,
+                       B_PFULL = B_SFULL + 1, B_DQFULL = B_PFULL + 1, B_DQEMPTY = B_DQFULL + 1,
+                       B_DKVFULL = B_DQEMPTY + 1, B_DONE = B_DKVFULL + 1, NBAR = B_DONE + 1;
+  static constexpr uint32_t BAR_OFF = 0;
+  static constexpr uint32_t MISC_OFF = BAR_OFF + NBAR * 8;          // tmem slot, abort flag
+  static constexpr uint32_t STAT_OFF = (MISC_OFF + 16 + 15) / 16 * 16;  // [STAGES][2][128] f32
+  static constexpr uint32_t SMALL_END = STAT_OFF + STAGES * 2 * 128 * 4;
+  static constexpr uint32_t TILE_BASE = (SMALL_END + 1023) / 1024 * 1024;
+  static constexpr uint32_t K_OFF = TILE_BASE;
+  static constexpr uint32_t V_OFF = K_OFF + TILE;
+  static constexpr uint32_t Q_OFF = V_OFF + TILE;                 // [STAGES] tiles
+  static constexpr uint32_t DO_OFF = Q_OFF + STAGES * TILE;       // [STAGES] tiles
+  static constexpr uint32_t DS_OFF = DO_OFF + STAGES * TILE;      // 2 chunks (128 keys x 128 queries)
+  static constexpr uint32_t SMEM_ALLOC = DS_OFF + 2 * CHUNK;
+  // TMEM columns
+  static constexpr uint32_t TM_DK = 0, TM_DV = D, TM_S = 2 * D, TM_DP = 2 * D + 128;
+  static constexpr uint32_t TM_DQ = (D == 128) ? TM_DP : (2 * D + 256);  // D=128: aliases dP^T
+  static constexpr uint32_t TMEM_COLS = 512;
+  static constexpr int NTHREADS = 320;
+};
+
+struct BwdItem {
+  int b, hkv, j;
+  int i0;      // first Q tile visited
+  int ntiles;  // (query heads of the group) x (Q tiles visited)
+};
+
+__device__ __forceinline__ BwdItem bwd_decode(int item, const BwdParams& p) {
+  BwdItem it;
+  it.j = item % p.n_kv;
+  const int bh = item / p.n_kv;
+  it.b = bh / p.Hkv;
+  it.hkv = bh - it.b * p.Hkv;
+  it.i0 = p.causal ? it.j : 0;
+  it.ntiles = (p.H / p.Hkv) * (p.n_kv - it.i0);
+  return it;
+}
+
+// n-th (head, Q tile) pair of an item: heads of the group outer, tiles inner.
+__device__ __forceinline__ void bwd_tile(const BwdItem& it, const BwdParams& p, int n, int& h,
+                                         int& i) {
+  const int per = p.n_kv - it.i0;
+  const int g = n / per;
+  i = it.i0 + (n - g * per);
+  h = it.hkv * (p.H / p.Hkv) + g;
+}
+
+template <int D, bool BF16>
+__global__ void __launch_bounds__(320, 1)
+    fa_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                  const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
+                  const BwdParams p) {
+  using Ly = BwdLayout<D>;
+  using T = typename std::conditional<BF16, __nv_bfloat16, __half>::type;
+  constexpr uint32_t IDESC_SS = idesc_f16(BF16, 128, 128, false, false);  // S^T, dP^T
+  constexpr uint32_t IDESC_KN = idesc_f16(BF16, 128, D, false, true);     // dV (A tmem), dK
+  constexpr uint32_t IDESC_MN = idesc_f16(BF16, 128, D, true, true);      // dQ
+
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  const uint32_t base = smem_u32(smem_raw);
+  auto bar = [&](int i) -> uint32_t { return base + Ly::BAR_OFF + 8u * i; };
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem_raw + Ly::MISC_OFF);
+  AbortState* ab = reinterpret_cast<AbortState*>(smem_raw + Ly::MISC_OFF + 8);
+  float* stats = reinterpret_cast<float*>(smem_raw + Ly::STAT_OFF);
+  unsigned int* err = device_error_word();
+  const uint32_t warp = warp_id(), lane = lane_id();
+
+  // The swizzled operand tiles need a 1024-byte aligned shared window.
+  if (base & 1023u) {
+    if (threadIdx.x == 0) atomicCAS(err, 0u, 499u);
+    return;
+  }
+  const BwdItem it = bwd_decode(blockIdx.x, p);
+  if (threadIdx.x == 0) {
+    mbar_init(bar(Ly::B_KVFULL), 1);
+    for (int s = 0; s < Ly::STAGES; ++s) {
+      mbar_init(bar(Ly::B_QFULL + s), 32);
+      mbar_init(bar(Ly::B_QEMPTY + s), 1);
+    }
+    mbar_init(bar(Ly::B_SFULL), 1);
+    mbar_init(bar(Ly::B_PFULL), 128);
+    mbar_init(bar(Ly::B_DQFULL), 1);
+    mbar_init(bar(Ly::B_DQEMPTY), 128);
+    mbar_init(bar(Ly::B_DKVFULL), 1);
+    mbar_init(bar(Ly::B_DONE), 1);
+    ab->flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 8 && lane == 0) {
+    tma_prefetch_desc(&tmQ);
+    tma_prefetch_desc(&tmK);
+    tma_prefetch_desc(&tmV);
+    tma_prefetch_desc(&tmdO);
+  }
+  if (warp == 9) {
+    tmem_alloc(base + Ly::MISC_OFF, Ly::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const int ntiles = it.ntiles;
+
+  if (warp == 8) {
+    // ------------------------------------------------------------ producer (whole warp)
+    bool ok = true;
+    uint32_t issued[Ly::STAGES] = {0, 0};
+    if (lane == 0) {
+      mbar_arrive_expect_tx(bar(Ly::B_KVFULL), 2 * Ly::TILE);
+      for (int c = 0; c < Ly::KCH; ++c) {
+        tma_load_4d(base + Ly::K_OFF + c * Ly::CHUNK, &tmK, bar(Ly::B_KVFULL), c * 64, it.hkv,
+                    it.j * 128, it.b);
+        tma_load_4d(base + Ly::V_OFF + c * Ly::CHUNK, &tmV, bar(Ly::B_KVFULL), c * 64, it.hkv,
+                    it.j * 128, it.b);
+      }
+    }
+    uint32_t stage = 0, phase = 0;
+    for (int n = 0; n < ntiles; ++n) {
+      int h, i;
+      bwd_tile(it, p, n, h, i);
+      if (!mbar_wait_warp(bar(Ly::B_QEMPTY + stage), phase ^ 1u, ab, err, 401)) { ok = false; break; }
+      // LSE (pre-multiplied by log2 e) and Delta of the 128 query rows of tile i.
+      float* st = stats + stage * 256;
+      const size_t row0 = (static_cast<size_t>(it.b) * p.H + h) * p.L;
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int c = lane + 32 * u;
+        const int q = i * 128 + c;
+        const bool in = q < p.L;
+        st[c] = in ? p.LSE[row0 + q] * 1.4426950408889634f : 0.f;
+        st[128 + c] = in ? p.Delta[row0 + q] : 0.f;
+      }
+      if (lane == 0) {
+        mbar_arrive_expect_tx(bar(Ly::B_QFULL + stage), 2 * Ly::TILE);
+        for (int c = 0; c < Ly::KCH; ++c) {
+          tma_load_4d(base + Ly::Q_OFF + stage * Ly::TILE + c * Ly::CHUNK, &tmQ,
+                      bar(Ly::B_QFULL + stage), c * 64, h, i * 128, it.b);
+          tma_load_4d(base + Ly::DO_OFF + stage * Ly::TILE + c * Ly::CHUNK, &tmdO,
+                      bar(Ly::B_QFULL + stage), c * 64, h, i * 128, it.b);
+        }
+      } else {
+        mbar_arrive(bar(Ly::B_QFULL + stage));
+      }
+      ++issued[stage];
+      if (++stage == Ly::STAGES) {
+        stage = 0;
+        phase ^= 1u;
+      }
+    }
+    if (!ok && lane == 0) {
+      mbar_wait_drain(bar(Ly::B_KVFULL), 0);
+      for (int s = 0; s < Ly::STAGES; ++s)
+        if (issued[s] > 0) mbar_wait_drain(bar(Ly::B_QFULL + s), (issued[s] - 1) & 1);
+    }
+  } else if (warp == 9) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      bool ok = mbar_wait(bar(Ly::B_KVFULL), 0, ab, err, 501);
+      tc_fence_after();
+      uint32_t stage = 0, phase = 0;
+      const uint32_t ka = base + Ly::K_OFF, va = base + Ly::V_OFF, dsa = base + Ly::DS_OFF;
+      for (int n = 0; ok && n < ntiles; ++n) {
+        if (!mbar_wait(bar(Ly::B_QFULL + stage), phase, ab, err, 502)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t qa = base + Ly::Q_OFF + stage * Ly::TILE;
+        const uint32_t doa = base + Ly::DO_OFF + stage * Ly::TILE;
+        // S^T = K_j Q_i^T  (keys x queries)
+#pragma unroll
+        for (int k = 0; k < D / 16; ++k) {
+          const uint32_t off = (k >> 2) * Ly::CHUNK + (k & 3) * 32u;
+          mma_ss(tmem + Ly::TM_S, sdesc_sw128(ka + off, 16, 1024), sdesc_sw128(qa + off, 16, 1024),
+                 IDESC_SS, k > 0 ? 1u : 0u);
+        }
+        if (D == 128 && n > 0) {  // dQ of the previous tile lives where dP^T goes
+          if (!mbar_wait(bar(Ly::B_DQEMPTY), (n - 1) & 1, ab, err, 503)) { ok = false; break; }
+          tc_fence_after();
+        }
+        // dP^T = V_j dO_i^T
+#pragma unroll
+        for (int k = 0; k < D / 16; ++k) {
+          const uint32_t off = (k >> 2) * Ly::CHUNK + (k & 3) * 32u;
+          mma_ss(tmem + Ly::TM_DP, sdesc_sw128(va + off, 16, 1024),
+                 sdesc_sw128(doa + off, 16, 1024), IDESC_SS, k > 0 ? 1u : 0u);
+        }
+        tc_commit(bar(Ly::B_SFULL));
+        if (!mbar_wait(bar(Ly::B_PFULL), n & 1, ab, err, 504)) { ok = false; break; }
+        tc_fence_after();
+        // dV += P^T dO_i   (P^T from TMEM, dO_i as an MN-major B operand)
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+          mma_ts(tmem + Ly::TM_DV, tmem + Ly::TM_S + 8u * k,
+                 sdesc_sw128(doa + 2048u * k, Ly::CHUNK, 1024), IDESC_KN,
+                 (n > 0 || k > 0) ? 1u : 0u);
+        // dK += dS^T Q_i   (dS^T K-major in smem, Q_i MN-major)
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const uint32_t off = (k >> 2) * Ly::CHUNK + (k & 3) * 32u;
+          mma_ss(tmem + Ly::TM_DK, sdesc_sw128(dsa + off, 16, 1024),
+                 sdesc_sw128(qa + 2048u * k, Ly::CHUNK, 1024), IDESC_KN,
+                 (n > 0 || k > 0) ? 1u : 0u);
+        }
+        if (D != 128 && n > 0) {
+          if (!mbar_wait(bar(Ly::B_DQEMPTY), (n - 1) & 1, ab, err, 505)) { ok = false; break; }
+          tc_fence_after();
+        }
+        // dQ_i = dS K_j   (dS read MN-major from the dS^T tile, K_j MN-major)
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+          mma_ss(tmem + Ly::TM_DQ, sdesc_sw128(dsa + 2048u * k, Ly::CHUNK, 1024),
+                 sdesc_sw128(ka + 2048u * k, Ly::CHUNK, 1024), IDESC_MN, k > 0 ? 1u : 0u);
+        tc_commit(bar(Ly::B_DQFULL));
+        tc_commit(bar(Ly::B_QEMPTY + stage));
+        if (++stage == Ly::STAGES) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+      if (ok) tc_commit(bar(Ly::B_DKVFULL));
+      tc_commit(bar(Ly::B_DONE));
+      mbar_wait_drain(bar(Ly::B_DONE), 0);
+    }
+  } else if (warp < 4) {
+    // ------------------------------------------------------------ P^T / dS^T
+    const int r = threadIdx.x & 127;  // key row within the tile == TMEM lane
+    const int kr = it.j * 128 + r;
+    const uint32_t lane_off = ((warp & 3u) * 32u) << 16;
+    const uint32_t tS = tmem + lane_off + Ly::TM_S;
+    const uint32_t tP = tmem + lane_off + Ly::TM_DP;
+    const float sl2 = p.sl2;
+    uint8_t* ds_row = smem_raw + Ly::DS_OFF + r * 128;
+    bool ok = true;
+    uint32_t stage = 0;
+    for (int n = 0; n < ntiles; ++n) {
+      int h, i;
+      bwd_tile(it, p, n, h, i);
+      if (!mbar_wait_warp(bar(Ly::B_SFULL), n & 1, ab, err, 601)) { ok = false; break; }
+      tc_fence_after();
+      const float* st = stats + stage * 256;
+      const int q0 = i * 128;
+      // query columns [lo, hi) of this tile are visible to key kr
+      int lo = 0, hi = min(128, p.L - q0);
+      if (kr >= p.L) hi = 0;
+      if (p.causal) lo = max(0, kr - q0);
+#pragma unroll
+      for (int ch = 0; ch < 4; ++ch) {  // 32 query columns per chunk
+        uint32_t s[32], dp[32];
+        tmem_ld32(tS + 32 * ch, s);
+        tmem_ld32(tP + 32 * ch, dp);
+        tmem_ld_wait32(s);
+        tmem_ld_wait32(dp);
+        uint32_t pk[16], dk[16];
+#pragma unroll
+        for (int u = 0; u < 16; ++u) {
+          float pv[2], dv[2];
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const int cl = 2 * u + e, c = 32 * ch + cl;
+            float pp = ex2(fmaf(__uint_as_float(s[cl]), sl2, -st[c]));
+            pp = (c >= lo && c < hi) ? pp : 0.f;
+            pv[e] = pp;
+            dv[e] = pp * (__uint_as_float(dp[cl]) - st[128 + c]);
+          }
+          pk[u] = pack2<T>(pv[0], pv[1]);
+          dk[u] = pack2<T>(dv[0], dv[1]);
+        }
+        // P^T columns (16-bit pairs) overwrite S^T columns already read.
+        tmem_st16(tS + 16 * ch, pk);
+        // dS^T row r, queries 32*ch .. 32*ch+31: four swizzled 16-byte units.
+        uint8_t* chunk_row = ds_row + (ch >> 1) * Ly::CHUNK;
+#pragma unroll
+        for (int v = 0; v < 4; ++v) {
+          const int pos = ((ch & 1) * 4 + v) ^ (r & 7);
+          *reinterpret_cast<uint4*>(chunk_row + pos * 16) =
+              make_uint4(dk[4 * v], dk[4 * v + 1], dk[4 * v + 2], dk[4 * v + 3]);
+        }
+      }
+      tmem_st_wait();
+      fence_proxy_async_smem();
+      tc_fence_before();
+      mbar_arrive(bar(Ly::B_PFULL));
+      if (++stage == Ly::STAGES) stage = 0;
+    }
+    // dK epilogue: scale by 1/sqrt(D) and store row kr.
+    if (ok && mbar_wait_warp(bar(Ly::B_DKVFULL), 0, ab, err, 602)) {
+      tc_fence_after();
+      T* row = reinterpret_cast<T*>(p.dK) + ((static_cast<size_t>(it.b) * p.L + kr) * p.Hkv + it.hkv) * D;
+#pragma unroll
+      for (int cc = 0; cc < D / 32; ++cc) {
+        uint32_t o[32];
+        tmem_ld32(tmem + lane_off + Ly::TM_DK + 32 * cc, o);
+        tmem_ld_wait32(o);
+        uint32_t pk[16];
+#pragma unroll
+        for (int u = 0; u < 16; ++u)
+          pk[u] = pack2<T>(__uint_as_float(o[2 * u]) * p.scale, __uint_as_float(o[2 * u + 1]) * p.scale);
+        if (kr < p.L) {
+          uint4* dst = reinterpret_cast<uint4*>(row + 32 * cc);
+#pragma unroll
+          for (int u = 0; u < 4; ++u)
+            dst[u] = make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
+        }
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ dQ drain + dV epilogue
+    const int r = threadIdx.x & 127;  // query row within the Q tile == TMEM lane
+    const uint32_t lane_off = ((warp & 3u) * 32u) << 16;
+    const uint32_t tQ = tmem + lane_off + Ly::TM_DQ;
+    bool ok = true;
+    for (int n = 0; n < ntiles; ++n) {
+      int h, i;
+      bwd_tile(it, p, n, h, i);
+      if (!mbar_wait_warp(bar(Ly::B_DQFULL), n & 1, ab, err, 701)) { ok = false; break; }
+      tc_fence_after();
+      const int q = i * 128 + r;
+      // accumulator layout [B, H, D/4, Lpad, 4]: a warp's 32 rows of one
+      // 4-column group are 512 contiguous bytes.
+      float4* acc = reinterpret_cast<float4*>(p.dq_accum) +
+                    (static_cast<size_t>(it.b) * p.H + h) * (D / 4) * p.Lpad + q;
+#pragma unroll
+      for (int cc = 0; cc < D / 32; ++cc) {
+        uint32_t g[32];
+        tmem_ld32(tQ + 32 * cc, g);
+        tmem_ld_wait32(g);
+        if (q < p.L) {
+#pragma unroll
+          for (int c4 = 0; c4 < 8; ++c4)
+            atomicAdd(acc + static_cast<size_t>(8 * cc + c4) * p.Lpad,
+                      make_float4(__uint_as_float(g[4 * c4]), __uint_as_float(g[4 * c4 + 1]),
+                                  __uint_as_float(g[4 * c4 + 2]), __uint_as_float(g[4 * c4 + 3])));
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(bar(Ly::B_DQEMPTY));
+    }
+    if (ok && mbar_wait_warp(bar(Ly::B_DKVFULL), 0, ab, err, 702)) {
+      tc_fence_after();
+      const int kr = it.j * 128 + r;
+      T* row = reinterpret_cast<T*>(p.dV) + ((static_cast<size_t>(it.b) * p.L + kr) * p.Hkv + it.hkv) * D;
+#pragma unroll
+      for (int cc = 0; cc < D / 32; ++cc) {
+        uint32_t o[32];
+        tmem_ld32(tmem + lane_off + Ly::TM_DV + 32 * cc, o);
+        tmem_ld_wait32(o);
+        uint32_t pk[16];
+#pragma unroll
+        for (int u = 0; u < 16; ++u) pk[u] = pack2<T>(__uint_as_float(o[2 * u]), __uint_as_float(o[2 * u + 1]));
+        if (kr < p.L) {
+          uint4* dst = reinterpret_cast<uint4*>(row + 32 * cc);
+#pragma unroll
+          for (int u = 0; u < 4; ++u)
+            dst[u] = make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 9) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, Ly::TMEM_COLS);
+  }
+}
+
+// ---------------------------------------------------------------- preprocess
+// One CTA per (batch, 32-row chunk of the padded sequence).  Reads the
+// chunk's O and dO rows for every head (one contiguous block), reduces each
+// row in fp32, and writes Delta for each head as 32 contiguous floats.  When
+// an accumulator is given it also zeroes that chunk of it.
+template <int D, bool BF16>
+__global__ void __launch_bounds__(256)
+    fa_bwd_prep_kernel(const void* __restrict__ O, const void* __restrict__ dO,
+                       float* __restrict__ Delta, float* __restrict__ dq_accum, int B, int L, int H,
+                       int Lpad) {
+  using T = typename std::conditional<BF16, __nv_bfloat16, __half>::type;
+  constexpr int TPR = D / 8;  // threads per row (16 bytes each)
+  extern __shared__ float dsm[];  // [H][32]
+  const int chunks = Lpad / 32;
+  const int b = blockIdx.x / chunks;
+  const int l0 = (blockIdx.x - b * chunks) * 32;
+  const int nrow = max(0, min(32, L - l0)) * H;  // rows (l, h) with l < L
+  const uint4* o4 = reinterpret_cast<const uint4*>(O) + ((static_cast<size_t>(b) * L + l0) * H) * TPR;
+  const uint4* d4 = reinterpret_cast<const uint4*>(dO) + ((static_cast<size_t>(b) * L + l0) * H) * TPR;
+  const int sub = threadIdx.x % TPR;
+  for (int row = threadIdx.x / TPR; row < ((nrow + (256 / TPR) - 1) / (256 / TPR)) * (256 / TPR);
+       row += 256 / TPR) {
+    float acc = 0.f;
+    if (row < nrow) {
+      const uint4 a = o4[static_cast<size_t>(row) * TPR + sub];
+      const uint4 c = d4[static_cast<size_t>(row) * TPR + sub];
+      const T* ea = reinterpret_cast<const T*>(&a);
+      const T* ec = reinterpret_cast<const T*>(&c);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) acc = fmaf(static_cast<float>(ea[e]), static_cast<float>(ec[e]), acc);
+    }
+#pragma unroll
+    for (int off = TPR / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+    if (sub == 0 && row < nrow) {
+      const int l = row / H, h = row - l * H;
+      dsm[h * 32 + l] = acc;
+    }
+  }
+  __syncthreads();
+  const int nl = max(0, min(32, L - l0));
+  for (int idx = threadIdx.x; idx < H * 32; idx += 256) {
+    const int h = idx / 32, l = idx - h * 32;
+    if (l < nl) Delta[(static_cast<size_t>(b) * H + h) * L + l0 + l] = dsm[idx];
+  }
+  if (dq_accum) {
+    // [B, H, D/4, Lpad, 4]: for each (h, column group) the chunk is 32 float4.
+    float4* acc = reinterpret_cast<float4*>(dq_accum);
+    const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int idx = threadIdx.x; idx < H * (D / 4) * 32; idx += 256) {
+      const int seg = idx / 32, l = idx - seg * 32;  // seg = h * (D/4) + c4
+      const int h = seg / (D / 4), c4 = seg - h * (D / 4);
+      acc[((static_cast<size_t>(b) * H + h) * (D / 4) + c4) * Lpad + l0 + l] = z;
+    }
+  }
+}
+
+// ---------------------------------------------------------------- dQ post-process
+// One CTA per (batch, head, 64-row chunk): reads the accumulator chunk
+// (column groups of 64 contiguous float4), transposes through shared memory,
+// scales by 1/sqrt(D) and writes BSHD rows.
+template <int D, bool BF16>
+__global__ void __launch_bounds__(256)
+    fa_dq_convert_kernel(const float* __restrict__ dq_accum, void* __restrict__ dQ, int B, int L,
+                         int H, int Lpad, float scale) {
+  using T = typename std::conditional<BF16, __nv_bfloat16, __half>::type;
+  __shared__ float tile[64][D + 4];
+  const int chunks = Lpad / 64;
+  const int bh = blockIdx.x / chunks;
+  const int l0 = (blockIdx.x - bh * chunks) * 64;
+  const int b = bh / H, h = bh - b * H;
+  const float4* src = reinterpret_cast<const float4*>(dq_accum) + static_cast<size_t>(bh) * (D / 4) * Lpad + l0;
+  for (int idx = threadIdx.x; idx < (D / 4) * 64; idx += 256) {
+    const int c4 = idx / 64, l = idx - c4 * 64;
+    const float4 v = src[static_cast<size_t>(c4) * Lpad + l];
+    tile[l][4 * c4 + 0] = v.x;
+    tile[l][4 * c4 + 1] = v.y;
+    tile[l][4 * c4 + 2] = v.z;
+    tile[l][4 * c4 + 3] = v.w;
+  }
+  __syncthreads();
+  constexpr int UPR = D / 8;  // 16-byte units per output row
+  for (int idx = threadIdx.x; idx < 64 * UPR; idx += 256) {
+    const int l = idx / UPR, u = idx - l * UPR;
+    if (l0 + l >= L) continue;
+    uint32_t pk[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e)
+      pk[e] = pack2<T>(tile[l][8 * u + 2 * e] * scale, tile[l][8 * u + 2 * e + 1] * scale);
+    T* row = reinterpret_cast<T*>(dQ) + ((static_cast<size_t>(b) * L + l0 + l) * H + h) * D;
+    reinterpret_cast<uint4*>(row)[u] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+  }
+}
+
+}  // namespace fa

@@ -1,0 +1,428 @@
+// Forward tiled online-softmax attention for sm_103a.
+//
+// Method (page "使用 TileLang 在 AMD GPU 上快速开发高性能 Flash Attention",
+// sections "Q Tile 处理与缓存初始化", "K/V Tile 遍历与核心计算" and
+// "最终输出写回与Q tile 迭代"): each 128-row Q tile streams its K/V tiles,
+// keeps a running row max m and row sum l in fp32, rescales the output
+// accumulator when the max moves, turns scores into probabilities with the
+// scale folded into the exponent, down-casts P to the input type before the PV
+// product, and divides by l at the end.  Causal tiles past the diagonal are
+// never visited; K/V heads are shared by groups of query heads.
+//
+// GB300 design (not the page's): one persistent CTA per SM, 384 threads.
+//   warps 0-3  softmax warpgroup for Q tile 0 (thread i owns row i)
+//   warps 4-7  softmax warpgroup for Q tile 1
+//   warp  8    TMA producer: Q pair, then K_j, V_j into a ring of smem slots
+//   warp  9    TMEM allocator and the single tcgen05.mma issuing thread
+//   warps 10-11 idle (they complete the third warpgroup so registers can be
+//              moved to the softmax warpgroups with setmaxnreg)
+// A work item is (batch, head, pair of 128-row Q tiles).  S_t = Q_t K_j^T and
+// O_t += P_t V_j accumulate in tensor memory; P_t overwrites S_t in TMEM as
+// 16-bit values and is read from there by the PV MMA.  While warpgroup 0
+// turns S_0 into P_0 the tensor cores compute S_1 (and the reverse), so the
+// exponentials overlap the MMAs.  O is rescaled only when a row max grows by
+// more than 2^8 (in exp2 units); the stale max is used consistently for l and
+// O, so the final O / l is exact up to rounding.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "common.cuh"
+#include "ptx.cuh"
+
+namespace fa {
+
+struct FwdParams {
+  void* O;      // [B, L, H, D] fp16/bf16
+  float* LSE;   // [B, H, L] fp32, natural log
+  int B, L, H, Hkv, causal;
+  int n_kv;      // ceil(L / 128)
+  int n_qpairs;  // ceil(L / 256)
+  int n_items;   // B * H * n_qpairs
+  float sl2;     // log2(e) / sqrt(D)
+};
+
+template <int D>
+struct FwdLayout {
+  static constexpr int KCH = D / 64;              // 128-byte column chunks per row
+  static constexpr uint32_t CHUNK = 128u * 128u;  // 128 rows x 128 B
+  static constexpr uint32_t TILE = KCH * CHUNK;   // one 128 x D tile
+  static constexpr int STAGES = (D == 128) ? 4 : 8;
+  static constexpr uint32_t Q_OFF = 0;
+  static constexpr uint32_t RING_OFF = 2 * TILE;
+  static constexpr uint32_t BAR_OFF = RING_OFF + STAGES * TILE;
+  // barrier slots
+  static constexpr int B_QFULL = 0, B_QEMPTY = 1, B_KVFULL = 2, B_KVEMPTY = 2 + STAGES,
+                       B_SFULL = 2 + 2 * STAGES, B_PFULL = B_SFULL + 2, B_OFULL = B_PFULL + 2,
+                       B_OEMPTY = B_OFULL + 2, B_DONE = B_OEMPTY + 2, NBAR = B_DONE + 1;
+  static constexpr uint32_t MISC_OFF = BAR_OFF + NBAR * 8;
+  static constexpr uint32_t SMEM_USED = MISC_OFF + 16;
+  static constexpr uint32_t SMEM_ALLOC = SMEM_USED + 1024;  // slack for 1024-byte alignment
+  static constexpr uint32_t TM_S0 = 0, TM_S1 = 128, TM_O0 = 256, TM_O1 = 256 + D;
+  static constexpr uint32_t TMEM_COLS = 512;
+  static constexpr int NTHREADS = 384;
+  // setmaxnreg split: 2 x 128 x 208 + 128 x 88 = 384 x 168 (the launch allocation)
+  static constexpr uint32_t REGS_SOFTMAX = 208, REGS_OTHER = 88;
+};
+
+struct FwdItem {
+  int b, h, hkv, q0;
+  int n[2];  // KV tiles visited by Q tile 0 / 1 (0 = tile lies past L)
+};
+
+__device__ __forceinline__ FwdItem fwd_decode(int item, const FwdParams& p) {
+  FwdItem it;
+  const int bh = item / p.n_qpairs;
+  // Within a head, pairs run from the last (longest under causal) to the first.
+  const int qp = p.n_qpairs - 1 - (item - bh * p.n_qpairs);
+  it.b = bh / p.H;
+  it.h = bh - it.b * p.H;
+  it.hkv = it.h / (p.H / p.Hkv);
+  it.q0 = qp * 256;
+#pragma unroll
+  for (int t = 0; t < 2; ++t) {
+    const int lo = it.q0 + 128 * t;
+    if (lo >= p.L) it.n[t] = 0;
+    else it.n[t] = p.causal ? (lo / 128 + 1) : p.n_kv;
+  }
+  return it;
+}
+
+template <typename T>
+__device__ __forceinline__ uint32_t pack2(float lo, float hi);
+template <>
+__device__ __forceinline__ uint32_t pack2<__half>(float lo, float hi) {
+  __half2 v = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+template <>
+__device__ __forceinline__ uint32_t pack2<__nv_bfloat16>(float lo, float hi) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+template <int D, bool BF16>
+__global__ void __launch_bounds__(384, 1)
+    fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                  const __grid_constant__ CUtensorMap tmV, const FwdParams p) {
+  using Ly = FwdLayout<D>;
+  using T = typename std::conditional<BF16, __nv_bfloat16, __half>::type;
+  constexpr uint32_t IDESC_S = idesc_f16(BF16, 128, 128, false, false);
+  constexpr uint32_t IDESC_PV = idesc_f16(BF16, 128, D, false, true);
+
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* gbase = smem_raw + (base - raw);
+  auto bar = [&](int i) -> uint32_t { return base + Ly::BAR_OFF + 8u * i; };
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + Ly::MISC_OFF);
+  AbortState* ab = reinterpret_cast<AbortState*>(gbase + Ly::MISC_OFF + 8);
+  unsigned int* err = fwd_error_word();
+
+  const uint32_t warp = warp_id(), lane = lane_id();
+
+  if (threadIdx.x == 0) {
+    mbar_init(bar(Ly::B_QFULL), 1);
+    mbar_init(bar(Ly::B_QEMPTY), 1);
+    for (int s = 0; s < Ly::STAGES; ++s) {
+      mbar_init(bar(Ly::B_KVFULL + s), 1);
+      mbar_init(bar(Ly::B_KVEMPTY + s), 1);
+    }
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(bar(Ly::B_SFULL + t), 1);
+      mbar_init(bar(Ly::B_PFULL + t), 128);
+      mbar_init(bar(Ly::B_OFULL + t), 1);
+      mbar_init(bar(Ly::B_OEMPTY + t), 128);
+    }
+    mbar_init(bar(Ly::B_DONE), 1);
+    ab->flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 8 && lane == 0) {
+    tma_prefetch_desc(&tmQ);
+    tma_prefetch_desc(&tmK);
+    tma_prefetch_desc(&tmV);
+  }
+  if (warp == 9) {
+    tmem_alloc(base + Ly::MISC_OFF, Ly::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp >= 8) {
+    regs_dec<Ly::REGS_OTHER>();
+  if (warp == 8) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      uint32_t stage = 0, phase = 0, q_uses = 0;
+      uint32_t issued[Ly::STAGES];
+      for (int s = 0; s < Ly::STAGES; ++s) issued[s] = 0;
+      const uint64_t keep = policy_evict_last();
+      bool ok = true;
+      for (int item = blockIdx.x; ok && item < p.n_items; item += gridDim.x) {
+        const FwdItem it = fwd_decode(item, p);
+        if (q_uses > 0 && !mbar_wait(bar(Ly::B_QEMPTY), (q_uses - 1) & 1, ab, err, 101)) {
+          ok = false;
+          break;
+        }
+        mbar_arrive_expect_tx(bar(Ly::B_QFULL), 2 * Ly::TILE);
+        for (int t = 0; t < 2; ++t)
+          for (int c = 0; c < Ly::KCH; ++c)
+            tma_load_4d(base + Ly::Q_OFF + t * Ly::TILE + c * Ly::CHUNK, &tmQ, bar(Ly::B_QFULL),
+                        c * 64, it.h, it.q0 + 128 * t, it.b);
+        ++q_uses;
+        const int nmax = max(it.n[0], it.n[1]);
+        for (int j = 0; ok && j < nmax; ++j) {
+          for (int kv = 0; kv < 2; ++kv) {
+            if (!mbar_wait(bar(Ly::B_KVEMPTY + stage), phase ^ 1u, ab, err, 102)) {
+              ok = false;
+              break;
+            }
+            mbar_arrive_expect_tx(bar(Ly::B_KVFULL + stage), Ly::TILE);
+            const CUtensorMap* m = kv ? &tmV : &tmK;
+            for (int c = 0; c < Ly::KCH; ++c)
+              tma_load_4d_hint(base + Ly::RING_OFF + stage * Ly::TILE + c * Ly::CHUNK, m,
+                               bar(Ly::B_KVFULL + stage), c * 64, it.hkv, j * 128, it.b, keep);
+            ++issued[stage];
+            if (++stage == Ly::STAGES) {
+              stage = 0;
+              phase ^= 1u;
+            }
+          }
+        }
+      }
+      if (!ok) {
+        // Unwinding: let copies already in flight land before the CTA exits.
+        if (q_uses > 0) mbar_wait_drain(bar(Ly::B_QFULL), (q_uses - 1) & 1);
+        for (int s = 0; s < Ly::STAGES; ++s)
+          if (issued[s] > 0) mbar_wait_drain(bar(Ly::B_KVFULL + s), (issued[s] - 1) & 1);
+      }
+    }
+  } else if (warp == 9) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      uint32_t stage = 0, phase = 0, q_cnt = 0;
+      uint32_t p_cnt[2] = {0, 0}, o_uses[2] = {0, 0};
+      bool ok = true;
+      const uint32_t tS[2] = {tmem + Ly::TM_S0, tmem + Ly::TM_S1};
+      const uint32_t tO[2] = {tmem + Ly::TM_O0, tmem + Ly::TM_O1};
+
+      auto issue_s = [&](int t, uint32_t kslot) {
+        const uint32_t qa = base + Ly::Q_OFF + t * Ly::TILE;
+        const uint32_t ka = base + Ly::RING_OFF + kslot * Ly::TILE;
+#pragma unroll
+        for (int k = 0; k < D / 16; ++k) {
+          const uint32_t off = (k >> 2) * Ly::CHUNK + (k & 3) * 32u;
+          mma_ss(tS[t], sdesc_sw128(qa + off, 16, 1024), sdesc_sw128(ka + off, 16, 1024), IDESC_S,
+                 k > 0 ? 1u : 0u);
+        }
+      };
+      auto issue_pv = [&](int t, uint32_t vslot, bool acc) {
+        const uint32_t va = base + Ly::RING_OFF + vslot * Ly::TILE;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          mma_ts(tO[t], tS[t] + 8u * k, sdesc_sw128(va + 2048u * k, Ly::CHUNK, 1024), IDESC_PV,
+                 (acc || k > 0) ? 1u : 0u);
+        }
+      };
+      auto take = [&](uint32_t& slot, unsigned int site) -> bool {
+        slot = stage;
+        if (!mbar_wait(bar(Ly::B_KVFULL + stage), phase, ab, err, site)) return false;
+        if (++stage == Ly::STAGES) {
+          stage = 0;
+          phase ^= 1u;
+        }
+        tc_fence_after();
+        return true;
+      };
+
+      for (int item = blockIdx.x; ok && item < p.n_items; item += gridDim.x) {
+        const FwdItem it = fwd_decode(item, p);
+        const int nmax = max(it.n[0], it.n[1]);
+        if (!mbar_wait(bar(Ly::B_QFULL), q_cnt & 1, ab, err, 201)) { ok = false; break; }
+        ++q_cnt;
+        tc_fence_after();
+        uint32_t kslot;
+        if (!take(kslot, 202)) { ok = false; break; }
+        for (int t = 0; t < 2; ++t)
+          if (it.n[t] > 0) {
+            issue_s(t, kslot);
+            tc_commit(bar(Ly::B_SFULL + t));
+          }
+        tc_commit(bar(Ly::B_KVEMPTY + kslot));
+        for (int j = 0; ok && j < nmax; ++j) {
+          uint32_t vslot, kslot1 = 0;
+          bool k_ready = false;
+          if (!take(vslot, 203)) { ok = false; break; }
+          for (int t = 0; t < 2; ++t) {
+            if (j < it.n[t]) {
+              if (j == 0 && o_uses[t] > 0 &&
+                  !mbar_wait(bar(Ly::B_OEMPTY + t), (o_uses[t] - 1) & 1, ab, err, 204)) {
+                ok = false;
+                break;
+              }
+              if (!mbar_wait(bar(Ly::B_PFULL + t), p_cnt[t] & 1, ab, err, 205)) { ok = false; break; }
+              ++p_cnt[t];
+              tc_fence_after();
+              issue_pv(t, vslot, j > 0);
+              if (j == it.n[t] - 1) {
+                tc_commit(bar(Ly::B_OFULL + t));
+                ++o_uses[t];
+              }
+            }
+            if (j + 1 < it.n[t]) {
+              if (!k_ready) {
+                if (!take(kslot1, 206)) { ok = false; break; }
+                k_ready = true;
+              }
+              issue_s(t, kslot1);
+              tc_commit(bar(Ly::B_SFULL + t));
+            }
+          }
+          if (!ok) break;
+          tc_commit(bar(Ly::B_KVEMPTY + vslot));
+          if (k_ready) tc_commit(bar(Ly::B_KVEMPTY + kslot1));
+        }
+        if (!ok) break;
+        tc_commit(bar(Ly::B_QEMPTY));
+      }
+      // Every MMA issued by this thread completes before TMEM is released.
+      tc_commit(bar(Ly::B_DONE));
+      mbar_wait_drain(bar(Ly::B_DONE), 0);
+    }
+  }
+    __syncwarp();
+    regs_inc<168>();
+  } else {
+    regs_inc<Ly::REGS_SOFTMAX>();
+    // ------------------------------------------------------------ softmax
+    const int t = warp >> 2;                       // Q tile of this warpgroup
+    const int r = threadIdx.x & 127;               // row within the tile == TMEM lane
+    const uint32_t lane_off = ((warp & 3u) * 32u) << 16;
+    const uint32_t tS = tmem + lane_off + (t ? Ly::TM_S1 : Ly::TM_S0);
+    const uint32_t tO = tmem + lane_off + (t ? Ly::TM_O1 : Ly::TM_O0);
+    const float sl2 = p.sl2;
+    uint32_t s_cnt = 0, o_cnt = 0;
+    bool ok = true;
+    for (int item = blockIdx.x; ok && item < p.n_items; item += gridDim.x) {
+      const FwdItem it = fwd_decode(item, p);
+      const int n = it.n[t];
+      if (n == 0) continue;
+      const int tile_lo = it.q0 + 128 * t;
+      const int q = tile_lo + r;
+      float m = -INFINITY, l = 0.f;
+      for (int j = 0; j < n; ++j) {
+        if (!mbar_wait_warp(bar(Ly::B_SFULL + t), s_cnt & 1, ab, err, 301)) { ok = false; break; }
+        ++s_cnt;
+        tc_fence_after();
+        uint32_t sr[128];
+        tmem_ld32(tS + 0, sr);
+        tmem_ld32(tS + 32, sr + 32);
+        tmem_ld32(tS + 64, sr + 64);
+        tmem_ld32(tS + 96, sr + 96);
+        tmem_ld_wait32(sr);
+        tmem_ld_wait32(sr + 32);
+        tmem_ld_wait32(sr + 64);
+        tmem_ld_wait32(sr + 96);
+        const int k0 = j * 128;
+        const bool need_mask = (k0 + 128 > p.L) || (p.causal && k0 + 127 > tile_lo);
+        float mx = -INFINITY;
+        if (need_mask) {
+          const int lim = p.causal ? min(q + 1, p.L) : p.L;  // keys [0, lim) are visible
+#pragma unroll
+          for (int c = 0; c < 128; ++c) {
+            if (k0 + c >= lim) sr[c] = __float_as_uint(-INFINITY);
+            mx = fmaxf(mx, __uint_as_float(sr[c]));
+          }
+        } else {
+#pragma unroll
+          for (int c = 0; c < 128; ++c) mx = fmaxf(mx, __uint_as_float(sr[c]));
+        }
+        const float m_new = fmaxf(m, mx);
+        if (j == 0) {
+          m = m_new;
+        } else {
+          const bool grow = (m_new - m) * sl2 > 8.0f;
+          if (__any_sync(0xffffffffu, grow)) {
+            // Rescale this warp's O rows (PV of the previous tile has completed:
+            // the commit that signalled S of this tile covers it).
+            const float alpha = ex2((m - m_new) * sl2);
+            m = m_new;
+            l *= alpha;
+#pragma unroll
+            for (int cc = 0; cc < D / 32; ++cc) {
+              uint32_t o[32];
+              tmem_ld32(tO + 32 * cc, o);
+              tmem_ld_wait32(o);
+#pragma unroll
+              for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+              tmem_st32(tO + 32 * cc, o);
+            }
+          }
+        }
+        const float mb = m * sl2;
+        float rs = 0.f;
+#pragma unroll
+        for (int h2 = 0; h2 < 2; ++h2) {
+          uint32_t pk[32];
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            const float p0 = ex2(fmaf(__uint_as_float(sr[64 * h2 + 2 * i]), sl2, -mb));
+            const float p1 = ex2(fmaf(__uint_as_float(sr[64 * h2 + 2 * i + 1]), sl2, -mb));
+            rs += p0 + p1;
+            pk[i] = pack2<T>(p0, p1);
+          }
+          tmem_st32(tS + 32 * h2, pk);
+        }
+        l += rs;
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(bar(Ly::B_PFULL + t));
+      }
+      if (!ok) break;
+      // ---- epilogue: O / l, LSE
+      if (!mbar_wait_warp(bar(Ly::B_OFULL + t), o_cnt & 1, ab, err, 302)) { ok = false; break; }
+      ++o_cnt;
+      tc_fence_after();
+      const float inv = l > 0.f ? 1.f / l : 0.f;
+      T* orow = reinterpret_cast<T*>(p.O) + ((static_cast<size_t>(it.b) * p.L + q) * p.H + it.h) * D;
+#pragma unroll
+      for (int cc = 0; cc < D / 32; ++cc) {
+        uint32_t o[32];
+        tmem_ld32(tO + 32 * cc, o);
+        tmem_ld_wait32(o);
+        uint32_t pk[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+          pk[i] = pack2<T>(__uint_as_float(o[2 * i]) * inv, __uint_as_float(o[2 * i + 1]) * inv);
+        if (q < p.L) {
+          uint4* dst = reinterpret_cast<uint4*>(orow + 32 * cc);
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+            dst[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+        }
+      }
+      if (q < p.L)
+        p.LSE[(static_cast<size_t>(it.b) * p.H + it.h) * p.L + q] =
+            (m * sl2 + __log2f(l)) * 0.6931471805599453f;
+      tc_fence_before();
+      mbar_arrive(bar(Ly::B_OEMPTY + t));
+    }
+    __syncwarp();
+    regs_dec<168>();
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 9) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, Ly::TMEM_COLS);
+  }
+}
+
+}  // namespace fa

@@ -1,0 +1,24 @@
+// Internal (C++) entry points between the C ABI and the kernel units.
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include "../../include/fa.h"
+
+namespace fa {
+
+fa_status run_fwd(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int L,
+                  int H, int Hkv, int D, int causal, int dtype, cudaStream_t s);
+unsigned int fwd_read_error(cudaStream_t s);
+
+fa_status run_bwd_prep(const void* O, const void* dO, float* Delta, float* dq_accum, int B, int L,
+                       int H, int D, int dtype, cudaStream_t s);
+fa_status run_bwd(const void* Q, const void* K, const void* V, const void* dO, const float* LSE,
+                  const float* Delta, void* dQ, void* dK, void* dV, float* dq_accum,
+                  int zero_accum, int B, int L, int H, int Hkv, int D, int causal, int dtype,
+                  cudaStream_t s);
+unsigned int bwd_read_error(cudaStream_t s);
+
+inline int padded_len(int L) { return (L + 127) / 128 * 128; }
+
+}  // namespace fa
