@@ -1,0 +1,411 @@
+#!/usr/bin/env python3
+"""Benchmark: attention forward + backward TFLOP/s at B8 H32 L4096 D128 fp16.
+
+One step = the whole hot path on one batch of synthetic inputs already in
+HBM: forward (O, LSE), Delta preprocess (+ dQ accumulator zeroing), the
+backward main pass (dK, dV, dQ accumulator) and the dQ post-process.  FLOPs
+follow the usual convention: 4*B*H*L^2*D for the forward, 2.5x that for the
+backward, halved under causal masking.  Prints one JSON line (rank 0).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--causal]
+
+``--impl reference`` times the fp64 CPU oracle on the host cores on a bounded
+sample of the same workload (one (batch, head) unit's forward + backward per
+step) and prints the same metric.  Under torchrun (N > 1) every rank runs its
+own replica (independent batches, no collective on the data path) and the
+reported time is the maximum over ranks.
+"""
+
+from __future__ import annotations
+
+import argparse
+import csv
+import hashlib
+import io
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+WORK = dict(B=8, L=4096, H=32, Hkv=32, D=128, dtype="fp16")
+METRIC = "attention fwd/bwd TFLOP/s (fp16 B8 H32 L4096 D128) and % of GB300 TC peak"
+KERNEL_SOURCES = ["tiled_attention_fa_gb300/csrc/ptx.cuh", "tiled_attention_fa_gb300/csrc/common.cuh",
+                  "tiled_attention_fa_gb300/csrc/fwd.cuh", "tiled_attention_fa_gb300/csrc/bwd.cuh"]
+
+
+def fwd_flops(B, H, L, D, causal):
+    f = 4.0 * B * H * L * L * D
+    return f / 2 if causal else f
+
+
+def step_flops(B, H, L, D, causal):
+    return 3.5 * fwd_flops(B, H, L, D, causal)   # forward + 2.5x backward
+
+
+def peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as fh:
+            m = json.load(fh)
+        return m["bf16_tflops"], m["bf16_tflops_sustained"], m["hbm_gbs"], "measured"
+    except (OSError, KeyError, ValueError):
+        return 1900.0, 1700.0, 6800.0, "fallback"
+
+
+def source_hash():
+    h = hashlib.sha256()
+    for p in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, p), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(kernel):
+    """DRAM bytes per launch of ``kernel`` from the committed ncu summary, or
+    None when absent or taken on different kernel sources."""
+    path = os.path.join(ROOT, "profiles", "traffic.txt")
+    try:
+        with open(path) as fh:
+            for line in fh:
+                f = dict(kv.split("=", 1) for kv in line.split() if "=" in kv)
+                if f.get("kernel") == kernel and f.get("src") == source_hash():
+                    return float(f["dram_bytes_per_launch"])
+    except OSError:
+        pass
+    return None
+
+
+# --------------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """nvidia-smi sampled every 100 ms while the timed region runs."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.tmp = None
+
+    def start(self):
+        self.tmp = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=self.tmp, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.tmp.flush()
+        self.tmp.seek(0)
+        rows = [r for r in csv.reader(io.StringIO(self.tmp.read())) if len(r) >= 9]
+        os.unlink(self.tmp.name)
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            try:
+                sm.append(float(r[1]))
+                mx.append(float(r[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names, r[5:9]):
+                if val.strip().lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# --------------------------------------------------------------------- oracle timing
+
+def blas_threads():
+    """Threads the host BLAS uses (OpenBLAS query when the library exposes one)."""
+    import ctypes
+    import numpy as np  # noqa: F401  (loads numpy's BLAS)
+    try:
+        with open("/proc/self/maps") as fh:
+            libs = {ln.split()[-1] for ln in fh if "openblas" in ln.lower() and "/" in ln}
+    except OSError:
+        libs = set()
+    for lib in libs:
+        try:
+            h = ctypes.CDLL(lib)
+        except OSError:
+            continue
+        for name in ("openblas_get_num_threads", "openblas_get_num_threads64_",
+                     "scipy_openblas_get_num_threads64_", "scipy_openblas_get_num_threads"):
+            fn = getattr(h, name, None)
+            if fn is not None:
+                return int(fn())
+    return len(os.sched_getaffinity(0))
+
+
+def time_oracle_units(q, k, v, do, causal, n_units, budget_s):
+    """Run the oracle's forward+backward on (b, h) units until ``n_units`` or
+    ``budget_s`` seconds; returns (units done, seconds)."""
+    from oracle import fa_oracle as orc
+    B, L, H, D = q.shape
+    Hkv = k.shape[2]
+    done, t0 = 0, time.perf_counter()
+    for u in range(n_units):
+        b, h = u % B, (u // B) % H
+        hk = orc.kv_head(h, H, Hkv)
+        orc.unit_backward(q[b, :, h], k[b, :, hk], v[b, :, hk], do[b, :, h], causal)
+        done += 1
+        if time.perf_counter() - t0 > budget_s:
+            break
+    return done, time.perf_counter() - t0
+
+
+def cpu_unit_inputs(seed=0):
+    """One (b, h) unit of the workload, [1, L, 1, D] float64 host arrays (same recipe as the tests)."""
+    from tiled_attention_fa_gb300.inputs import make_qkv
+    q, k, v, do = make_qkv(1, WORK["L"], 1, 1, WORK["D"], WORK["dtype"], seed=seed)
+    return tuple(t.double().numpy() for t in (q, k, v, do))
+
+
+# --------------------------------------------------------------------- arms
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def reference_arm(args):
+    world, rank, _ = dist_setup()
+    if rank != 0:
+        return 0
+    L, D = WORK["L"], WORK["D"]
+    qs, ks, vs, dos = cpu_unit_inputs()
+    flops_unit = step_flops(1, 1, L, D, args.causal)
+    time_oracle_units(qs, ks, vs, dos, args.causal, args.warmup, 1e9)
+    n, secs = time_oracle_units(qs, ks, vs, dos, args.causal, args.steps, 1e9)
+    value = n * flops_unit / secs / 1e12
+    cores = blas_threads()
+    sample = (f"oracle fp64 forward+backward of one (batch, head) unit per step "
+              f"(L={L}, D={D}, {'causal' if args.causal else 'non-causal'}), {n} steps")
+    out = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
+        "n_gpus": world, "steps": n, "warmup": args.warmup,
+        "ms_per_step": secs / n * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": config_dict(args, world),
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(out), flush=True)
+    return 0
+
+
+def config_dict(args, world):
+    B, L, H, Hkv, D = WORK["B"], WORK["L"], WORK["H"], WORK["Hkv"], WORK["D"]
+    return {"workload": f"attention fwd+bwd B{B} H{H} Hkv{Hkv} L{L} D{D} fp16 "
+                        f"{'causal' if args.causal else 'non-causal'}",
+            "B": B, "L": L, "H": H, "Hkv": Hkv, "D": D, "causal": bool(args.causal),
+            "per_gpu_batch": B, "global_batch": B * world, "parallelism": f"replicas x{world}",
+            "l2": "inputs larger than L2 (Q, K, V, dO 268 MB each)"}
+
+
+def ours_arm(args):
+    import torch
+    import torch.distributed as dist
+    import tiled_attention_fa_gb300 as fa
+    from tiled_attention_fa_gb300 import _lib
+
+    world, rank, local = dist_setup()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=dev)
+    _lib.load()  # fails loudly without the built library
+
+    B, L, H, Hkv, D = WORK["B"], WORK["L"], WORK["H"], WORK["Hkv"], WORK["D"]
+    causal = bool(args.causal)
+    dt = torch.float16
+    g = torch.Generator(device=dev).manual_seed(1234 + rank)
+    q = torch.randn(B, L, H, D, device=dev, dtype=dt, generator=g)
+    k = torch.randn(B, L, Hkv, D, device=dev, dtype=dt, generator=g)
+    v = torch.randn(B, L, Hkv, D, device=dev, dtype=dt, generator=g)
+    do = torch.randn(B, L, H, D, device=dev, dtype=dt, generator=g)
+    o = torch.empty_like(q)
+    lse = torch.empty(B, H, L, device=dev, dtype=torch.float32)
+    delta = torch.empty_like(lse)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    acc = fa.alloc_workspace(B, L, H, D, dev)
+    stream = torch.cuda.current_stream()
+
+    def step(ev=None):
+        if ev:
+            ev[0].record(stream)
+        fa.fwd(q, k, v, causal, out=o, lse=lse, stream=stream)
+        if ev:
+            ev[1].record(stream)
+        fa.bwd_preprocess(o, do, delta=delta, dq_accum=acc, stream=stream)
+        if ev:
+            ev[2].record(stream)
+        fa.bwd_main(q, k, v, do, lse, delta, acc, causal, dk=dk, dv=dv, accum_zeroed=True,
+                    stream=stream)
+        if ev:
+            ev[3].record(stream)
+        fa.bwd_postprocess(acc, dq, stream=stream)
+        if ev:
+            ev[4].record(stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    fa.check_device_error()
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    sampler = ClockSampler(local)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    sampler.start()
+    t_start.record(stream)
+    for i in range(args.steps):
+        step(evs[i])
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    clocks = sampler.stop()
+    fa.check_device_error()
+    ms = t_start.elapsed_time(t_end)
+    if world > 1:
+        t = torch.tensor([ms], device=dev, dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    ms_per_step = ms / args.steps
+
+    names = ["fa_fwd_kernel", "fa_bwd_prep_kernel", "fa_bwd_kernel", "fa_dq_convert_kernel"]
+    kms = {n: statistics.mean(e[i].elapsed_time(e[i + 1]) for e in evs) for i, n in enumerate(names)}
+    f_fwd = fwd_flops(B, H, L, D, causal)
+    f_bwd = 2.5 * f_fwd
+    Lpad = (L + 127) // 128 * 128
+    prep_bytes = 2 * B * L * H * D * 2 + 4 * B * H * L + 4 * B * H * Lpad * D
+    conv_bytes = 4 * B * H * Lpad * D + 2 * B * L * H * D
+    burst, sustained, hbm, src = peaks()
+    kernels = {
+        "fa_fwd_kernel": {"ms": kms["fa_fwd_kernel"], "tflops": f_fwd / kms["fa_fwd_kernel"] / 1e9},
+        "fa_bwd_prep_kernel": {"ms": kms["fa_bwd_prep_kernel"],
+                               "gbs": prep_bytes / kms["fa_bwd_prep_kernel"] / 1e6},
+        "fa_bwd_kernel": {"ms": kms["fa_bwd_kernel"], "tflops": f_bwd / kms["fa_bwd_kernel"] / 1e9},
+        "fa_dq_convert_kernel": {"ms": kms["fa_dq_convert_kernel"],
+                                 "gbs": conv_bytes / kms["fa_dq_convert_kernel"] / 1e6},
+    }
+    kernels["fa_fwd_kernel"]["frac_of_sustained"] = kernels["fa_fwd_kernel"]["tflops"] / sustained
+    kernels["fa_bwd_kernel"]["frac_of_sustained"] = kernels["fa_bwd_kernel"]["tflops"] / sustained
+    dom = max(names, key=lambda n: kms[n])
+    if dom in ("fa_fwd_kernel", "fa_bwd_kernel"):
+        ach = kernels[dom]["tflops"]
+        roof = {"kernel": dom, "bound": "tensor", "achieved": ach, "peak": sustained,
+                "unit": "TFLOP/s", "frac": ach / sustained,
+                "peak_source": f"{src} bf16 sustained (fp16 dense rate equals bf16)",
+                "frac_of_burst": ach / burst}
+    else:
+        ach = kernels[dom]["gbs"]
+        roof = {"kernel": dom, "bound": "hbm", "achieved": ach, "peak": hbm, "unit": "GB/s",
+                "frac": ach / hbm, "peak_source": f"{src} copy bandwidth"}
+    roof["traffic"] = recorded_traffic(dom)
+
+    value = world * step_flops(B, H, L, D, causal) / (ms_per_step * 1e-3) / 1e12
+
+    # ---- end to end through the public API with host buffers
+    e2e = None
+    if not args.no_e2e:
+        runner = fa.HostRunner(B, L, H, Hkv, D, dt, causal, dev)
+        hq, hk, hv, hdo = (x.cpu().pin_memory() for x in (q, k, v, do))
+        runner.run(hq, hk, hv, hdo)
+        torch.cuda.synchronize()
+        n_e2e = max(3, min(args.steps, 10))
+        s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+        s0.record(stream)
+        for _ in range(n_e2e):
+            runner.run(hq, hk, hv, hdo, stream=stream)
+        s1.record(stream)
+        torch.cuda.synchronize()
+        ems = s0.elapsed_time(s1) / n_e2e
+        if world > 1:
+            t = torch.tensor([ems], device=dev, dtype=torch.float64)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            ems = float(t.item())
+        e2e = {"value": world * step_flops(B, H, L, D, causal) / (ems * 1e-3) / 1e12,
+               "unit": "TFLOP/s", "h2d_bytes_per_step": runner.h2d_bytes(),
+               "d2h_bytes_per_step": runner.d2h_bytes(), "ms_per_step": ems, "steps": n_e2e}
+        del runner
+
+    # ---- oracle on the host cores (rank 0, one GPU only)
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        uq, uk, uv, udo = cpu_unit_inputs()
+        n, secs = time_oracle_units(uq, uk, uv, udo, causal, 8, args.cpu_budget)
+        cpu = {"value": n * step_flops(1, 1, L, D, causal) / secs / 1e12, "unit": "TFLOP/s",
+               "cores": blas_threads(), "kind": "oracle",
+               "sample": f"{n} (batch, head) unit(s) of the workload, forward+backward in fp64 "
+                         f"({secs:.1f} s)"}
+
+    if rank == 0:
+        out = {
+            "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "fp16",
+            "data": "synthetic", "config": config_dict(args, world),
+            "frac_of_peak": {"burst": value / world / burst, "sustained": value / world / sustained,
+                             "source": src},
+            "kernels": kernels, "roofline": roof, "clocks": clocks, "e2e": e2e,
+            "cpu_baseline": cpu, "gpu_launches": 4 * args.steps,
+        }
+        print(json.dumps(out), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=30)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--causal", action="store_true", help="causal masking (default: non-causal)")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle work")
+    ap.add_argument("--batch", type=int, default=WORK["B"],
+                    help="batch size (smaller values only for profiling captures)")
+    args = ap.parse_args()
+    WORK["B"] = args.batch
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        return reference_arm(args)
+    return ours_arm(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

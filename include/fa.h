@@ -92,6 +92,22 @@ fa_status fa_bwd(const void* Q, const void* K, const void* V, const void* O, con
                  int dtype, void* stream);
 
 /*
+ * The two stages fa_bwd runs, for callers that schedule or time them apart:
+ *   fa_bwd_main        dK, dV (written in full) and the dQ accumulator (added
+ *                      into; it must hold zeros on entry unless zero_accum);
+ *   fa_bwd_postprocess dQ = dq_accum / sqrt(D), converted back to BSHD.
+ * Page "TileLang与机器学习训练：反向传播算子优化案例", section
+ * 算子拆分与流水线设计 (the core gradient stage and the post-processing stage
+ * that reorders the dQ gradient).  Arguments mean what they mean for fa_bwd.
+ */
+fa_status fa_bwd_main(const void* Q, const void* K, const void* V, const void* dO,
+                      const float* LSE, const float* Delta, void* dK, void* dV, float* dq_accum,
+                      int zero_accum, int B, int L, int H, int Hkv, int D, int causal, int dtype,
+                      void* stream);
+fa_status fa_bwd_postprocess(const float* dq_accum, void* dQ, int B, int L, int H, int D,
+                             int dtype, void* stream);
+
+/*
  * Synchronise `stream` and report whether any kernel of this library gave up
  * a bounded wait since the last check (FA_ERR_DEVICE_TIMEOUT; the word is then
  * cleared).  Kernels never trap or spin forever: a wait that exceeds about one

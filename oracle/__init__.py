@@ -5,6 +5,7 @@ from .fa_oracle import (  # noqa: F401
     bwd_preprocess,
     forward,
     kv_head,
+    storage_round,
     unit_backward,
     unit_forward,
     unit_scores,

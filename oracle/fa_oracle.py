@@ -35,6 +35,11 @@ softmax, no fusion):
   reading used here is the per-row dot product that the softmax gradient
   needs.
 
+* Delta is formed from the stored forward output.  The pages' pipeline keeps
+  the forward Output tensor in the input dtype (fp16 in the printed kernel)
+  and the preprocess reads that tensor; ``o_round`` lets the backward round
+  its own O to that storage format before forming Delta (None = exact O).
+
 * Backward (the page elides every step after the dV product): the analytic
   gradient of O = softmax(S) V,
 
@@ -62,6 +67,7 @@ __all__ = [
     "forward",
     "backward",
     "bwd_preprocess",
+    "storage_round",
 ]
 
 
@@ -70,6 +76,26 @@ def kv_head(h: int, H: int, Hkv: int) -> int:
     if H % Hkv != 0:
         raise ValueError(f"H={H} is not a multiple of Hkv={Hkv}")
     return h // (H // Hkv)
+
+
+def storage_round(x: np.ndarray, fmt) -> np.ndarray:
+    """Round float64 values to a 16-bit storage format and back.
+
+    fmt None: unchanged.  Otherwise the value is rounded to binary32 first and
+    then to the 16-bit format with round-to-nearest-even -- the two steps a
+    kernel takes when it stores an fp32 result: "fp16" is IEEE binary16
+    (numpy's cast), "bf16" is bfloat16, the upper 16 bits of a binary32.
+    """
+    x = np.asarray(x, dtype=np.float64)
+    if fmt is None:
+        return x
+    if fmt == "fp16":
+        return x.astype(np.float32).astype(np.float16).astype(np.float64)
+    if fmt == "bf16":
+        b = x.astype(np.float32).view(np.uint32).astype(np.uint64)
+        b = (b + 0x7FFF + ((b >> 16) & 1)) & 0xFFFF0000
+        return b.astype(np.uint32).view(np.float32).astype(np.float64)
+    raise ValueError(f"unknown storage format {fmt!r}")
 
 
 def _as64(x) -> np.ndarray:
@@ -126,11 +152,13 @@ def unit_forward(q_bh, k_bh, v_bh, causal: bool, rows=None, panel: int = 4096):
     return np.concatenate(outs_o), np.concatenate(outs_l)
 
 
-def unit_backward(q_bh, k_bh, v_bh, do_bh, causal: bool, panel: int = 4096):
+def unit_backward(q_bh, k_bh, v_bh, do_bh, causal: bool, panel: int = 4096, o_round=None):
     """Gradients of one (b, h) pair against its K/V head.
 
     Returns (dQ [L, D], dK [L, D], dV [L, D], Delta [L], O [L, D], LSE [L]).
     The oracle recomputes its own O and Delta; nothing comes from a kernel.
+    ``o_round`` (None, "fp16", "bf16") is the storage format of the O that
+    Delta is formed from.
     """
     q_bh, k_bh, v_bh, do_bh = (_as64(x) for x in (q_bh, k_bh, v_bh, do_bh))
     L, D = q_bh.shape
@@ -151,7 +179,7 @@ def unit_backward(q_bh, k_bh, v_bh, do_bh, causal: bool, panel: int = 4096):
         o[r] = O
         lse[r] = m + np.log(s)
         dO = do_bh[r]
-        dl = (O * dO).sum(axis=1)               # Delta_i = sum_d O_id dO_id
+        dl = (storage_round(O, o_round) * dO).sum(axis=1)   # Delta_i = sum_d O_id dO_id
         delta[r] = dl
         dv += P.T @ dO                          # dV = P^T dO
         dP = dO @ v_bh.T                        # dP = dO V^T
@@ -186,11 +214,11 @@ def bwd_preprocess(o, do):
     return np.einsum("blhd,blhd->bhl", o, do)
 
 
-def backward(q, k, v, do, causal: bool):
+def backward(q, k, v, do, causal: bool, o_round=None):
     """Full backward over BSHD tensors.
 
     Returns dQ [B, L, H, D], dK [B, L, Hkv, D], dV [B, L, Hkv, D],
-    Delta [B, H, L] (from the oracle's own O).
+    Delta [B, H, L] (from the oracle's own O, rounded to ``o_round`` if given).
     """
     q, k, v, do = _as64(q), _as64(k), _as64(v), _as64(do)
     B, L, H, D = q.shape
@@ -203,7 +231,8 @@ def backward(q, k, v, do, causal: bool):
         for h in range(H):
             hk = kv_head(h, H, Hkv)
             gq, gk, gv, dl, _, _ = unit_backward(
-                q[b, :, h, :], k[b, :, hk, :], v[b, :, hk, :], do[b, :, h, :], causal)
+                q[b, :, h, :], k[b, :, hk, :], v[b, :, hk, :], do[b, :, h, :], causal,
+                o_round=o_round)
             dq[b, :, h, :] = gq
             dk[b, :, hk, :] += gk                 # group heads sum into their KV head
             dv[b, :, hk, :] += gv

@@ -46,3 +46,4 @@ def oracle_units_fwd(q, k, v, causal, units):
         hk = orc.kv_head(h, H, Hkv)
         out[(b, h)] = orc.unit_forward(q[b, :, h], k[b, :, hk], v[b, :, hk], causal)
     return out
+

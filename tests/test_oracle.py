@@ -404,3 +404,37 @@ def test_planted_backward_mistakes_are_caught():
     assert _backward_pins(orc.unit_backward), "pins must pass on the oracle itself"
     for kind in ("dv_untransposed", "no_delta", "dq_unscaled", "dk_untransposed"):
         assert not _backward_pins(_mutant_backward(kind)), f"planted mistake {kind!r} not caught"
+
+
+# ---------------------------------------------------------------- storage rounding
+
+@pytest.mark.parametrize("fmt,tdt", [("fp16", torch.float16), ("bf16", torch.bfloat16)])
+def test_storage_round_matches_torch_casts(fmt, tdt):
+    rng = np.random.default_rng(70)
+    x = rng.standard_normal(20000) * np.exp(rng.uniform(-8, 8, 20000))
+    want = torch.tensor(x, dtype=torch.float32).to(tdt).double().numpy()
+    np.testing.assert_array_equal(orc.storage_round(x, fmt), want)
+
+
+def test_storage_round_ties_and_identity():
+    # bf16 keeps 8 significant bits: 1 + 2^-8 is a tie between 1 and 1 + 2^-7 -> even (1.0);
+    # 1 + 3 * 2^-8 is a tie between 1 + 2^-7 and 1 + 2^-6 -> even (1 + 2^-6).
+    assert orc.storage_round(np.array([1 + 2.0 ** -8]), "bf16")[0] == 1.0
+    assert orc.storage_round(np.array([1 + 3 * 2.0 ** -8]), "bf16")[0] == 1 + 2.0 ** -6
+    assert orc.storage_round(np.array([1 + 2.0 ** -11]), "fp16")[0] == 1.0
+    vals = np.array([0.0, -2.5, 0.09375, 1024.0])
+    for fmt in ("fp16", "bf16", None):
+        np.testing.assert_array_equal(orc.storage_round(vals, fmt), vals)
+
+
+def test_rounded_delta_only_moves_delta():
+    # Rounding O before Delta leaves dV unchanged and moves Delta by at most the rounding.
+    B, L, H, D = 1, 40, 2, 16
+    q, k, v, do = (rnd((B, L, H, D), s) for s in (80, 81, 82, 83))
+    dq0, dk0, dv0, d0 = orc.backward(q, k, v, do, True)
+    dq1, dk1, dv1, d1 = orc.backward(q, k, v, do, True, o_round="bf16")
+    np.testing.assert_array_equal(dv0, dv1)
+    o, _ = orc.forward(q, k, v, True)
+    bound = 2.0 ** -9 * np.einsum("blhd->bhl", np.abs(o * do))
+    assert np.all(np.abs(d1 - d0) <= bound + 1e-15)
+    assert np.abs(d1 - d0).max() > 0

@@ -11,11 +11,13 @@ from .api import (  # noqa: F401
     alloc_workspace,
     attention_backward,
     bwd,
+    bwd_main,
+    bwd_postprocess,
     bwd_preprocess,
     check_device_error,
     fwd,
     workspace_size,
 )
 
-__all__ = ["fwd", "bwd_preprocess", "bwd", "attention_backward", "workspace_size",
+__all__ = ["fwd", "bwd_preprocess", "bwd", "attention_backward", "bwd_main", "bwd_postprocess", "workspace_size",
            "alloc_workspace", "check_device_error", "HostRunner"]

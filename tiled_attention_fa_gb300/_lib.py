@@ -26,6 +26,8 @@ _SIGS = {
     "fa_bwd_preprocess": ([_vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _vp], _i),
     "fa_bwd_workspace_size": ([_i, _i, _i, _i], ctypes.c_size_t),
     "fa_bwd": ([_vp] * 11 + [_i] * 8 + [_vp], _i),
+    "fa_bwd_main": ([_vp] * 9 + [_i] * 8 + [_vp], _i),
+    "fa_bwd_postprocess": ([_vp, _vp] + [_i] * 5 + [_vp], _i),
     "fa_check_device_error": ([_vp], _i),
     "fa_last_error_site": ([], ctypes.c_uint),
     "fa_status_string": ([_i], ctypes.c_char_p),

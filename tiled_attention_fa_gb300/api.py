@@ -122,6 +122,37 @@ def bwd(q, k, v, o, do, lse, delta, causal: bool = False, dq=None, dk=None, dv=N
     return dq, dk, dv
 
 
+def bwd_main(q, k, v, do, lse, delta, dq_accum, causal: bool = False, dk=None, dv=None,
+             accum_zeroed: bool = True, stream=None):
+    """Stage 2 alone: dK, dV and the fp32 dQ accumulator (added into)."""
+    B, L, H, D = q.shape
+    Hkv = k.shape[2]
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    for name, t in (("q", q), ("k", k), ("v", v), ("do", do), ("lse", lse), ("delta", delta),
+                    ("dk", dk), ("dv", dv), ("dq_accum", dq_accum)):
+        _need(t, name)
+    if dq_accum.numel() * 4 < workspace_size(B, L, H, D):
+        raise ValueError("dq_accum is smaller than workspace_size()")
+    st = _lib.load().fa_bwd_main(q.data_ptr(), k.data_ptr(), v.data_ptr(), do.data_ptr(),
+                                 lse.data_ptr(), delta.data_ptr(), dk.data_ptr(), dv.data_ptr(),
+                                 dq_accum.data_ptr(), 0 if accum_zeroed else 1, B, L, H, Hkv, D,
+                                 int(bool(causal)), _dtype_code(q), _stream(stream))
+    _lib.check("fa_bwd_main", st)
+    return dk, dv
+
+
+def bwd_postprocess(dq_accum, dq, stream=None):
+    """Stage 3 alone: dQ (BSHD, input dtype) from the fp32 accumulator."""
+    B, L, H, D = dq.shape
+    _need(dq, "dq")
+    _need(dq_accum, "dq_accum", dtype=torch.float32)
+    st = _lib.load().fa_bwd_postprocess(dq_accum.data_ptr(), dq.data_ptr(), B, L, H, D,
+                                        _dtype_code(dq), _stream(stream))
+    _lib.check("fa_bwd_postprocess", st)
+    return dq
+
+
 def attention_backward(q, k, v, o, lse, do, causal: bool = False, dq_accum=None, stream=None):
     """Preprocess + backward in one call (Delta computed here, accumulator zeroed in the same pass)."""
     B, L, H, D = q.shape

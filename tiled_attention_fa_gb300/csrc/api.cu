@@ -69,6 +69,27 @@ fa_status fa_bwd(const void* Q, const void* K, const void* V, const void* O, con
                      causal, dtype, static_cast<cudaStream_t>(stream));
 }
 
+fa_status fa_bwd_main(const void* Q, const void* K, const void* V, const void* dO,
+                      const float* LSE, const float* Delta, void* dK, void* dV, float* dq_accum,
+                      int zero_accum, int B, int L, int H, int Hkv, int D, int causal, int dtype,
+                      void* stream) {
+  fa_status st = check_shape(B, L, H, Hkv, D, dtype);
+  if (st != FA_OK) return st;
+  if (!ptr_ok(Q) || !ptr_ok(K) || !ptr_ok(V) || !ptr_ok(dO) || !ptr_ok(LSE) || !ptr_ok(Delta) ||
+      !ptr_ok(dK) || !ptr_ok(dV) || !ptr_ok(dq_accum))
+    return FA_ERR_INVALID_ARG;
+  return fa::run_bwd_main(Q, K, V, dO, LSE, Delta, dK, dV, dq_accum, zero_accum, B, L, H, Hkv, D,
+                          causal, dtype, static_cast<cudaStream_t>(stream));
+}
+
+fa_status fa_bwd_postprocess(const float* dq_accum, void* dQ, int B, int L, int H, int D,
+                             int dtype, void* stream) {
+  fa_status st = check_shape(B, L, H, H, D, dtype);
+  if (st != FA_OK) return st;
+  if (!ptr_ok(dq_accum) || !ptr_ok(dQ)) return FA_ERR_INVALID_ARG;
+  return fa::run_bwd_post(dq_accum, dQ, B, L, H, D, dtype, static_cast<cudaStream_t>(stream));
+}
+
 fa_status fa_check_device_error(void* stream) {
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const unsigned int a = fa::fwd_read_error(s);

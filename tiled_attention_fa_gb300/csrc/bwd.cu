@@ -35,7 +35,7 @@ fa_status run_bwd_prep(const void* O, const void* dO, float* Delta, float* dq_ac
 
 template <int D, bool BF16>
 static fa_status launch_bwd(const void* Q, const void* K, const void* V, const void* dO,
-                            const float* LSE, const float* Delta, void* dQ, void* dK, void* dV,
+                            const float* LSE, const float* Delta, void* dK, void* dV,
                             float* dq_accum, int zero_accum, int B, int L, int H, int Hkv,
                             int causal, cudaStream_t s) {
   using Ly = BwdLayout<D>;
@@ -73,26 +73,51 @@ static fa_status launch_bwd(const void* Q, const void* K, const void* V, const v
       cudaSuccess)
     return FA_ERR_CUDA;
   kern<<<p.n_items, Ly::NTHREADS, Ly::SMEM_ALLOC, s>>>(tq, tk, tv, tdo, p);
-  if (cudaGetLastError() != cudaSuccess) return FA_ERR_CUDA;
-  fa_dq_convert_kernel<D, BF16><<<B * H * (Lpad / 64), 256, 0, s>>>(dq_accum, dQ, B, L, H, Lpad,
-                                                                    p.scale);
   return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+template <int D, bool BF16>
+static fa_status launch_post(const float* dq_accum, void* dQ, int B, int L, int H, cudaStream_t s) {
+  const int Lpad = padded_len(L);
+  fa_dq_convert_kernel<D, BF16><<<B * H * (Lpad / 64), 256, 0, s>>>(
+      dq_accum, dQ, B, L, H, Lpad, 1.f / sqrtf(static_cast<float>(D)));
+  return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+fa_status run_bwd_main(const void* Q, const void* K, const void* V, const void* dO,
+                       const float* LSE, const float* Delta, void* dK, void* dV, float* dq_accum,
+                       int zero_accum, int B, int L, int H, int Hkv, int D, int causal, int dtype,
+                       cudaStream_t s) {
+  const bool bf16 = dtype == FA_BF16;
+  if (D == 64)
+    return bf16 ? launch_bwd<64, true>(Q, K, V, dO, LSE, Delta, dK, dV, dq_accum, zero_accum, B,
+                                       L, H, Hkv, causal, s)
+                : launch_bwd<64, false>(Q, K, V, dO, LSE, Delta, dK, dV, dq_accum, zero_accum, B,
+                                        L, H, Hkv, causal, s);
+  return bf16 ? launch_bwd<128, true>(Q, K, V, dO, LSE, Delta, dK, dV, dq_accum, zero_accum, B, L,
+                                      H, Hkv, causal, s)
+              : launch_bwd<128, false>(Q, K, V, dO, LSE, Delta, dK, dV, dq_accum, zero_accum, B,
+                                       L, H, Hkv, causal, s);
+}
+
+fa_status run_bwd_post(const float* dq_accum, void* dQ, int B, int L, int H, int D, int dtype,
+                       cudaStream_t s) {
+  const bool bf16 = dtype == FA_BF16;
+  if (D == 64)
+    return bf16 ? launch_post<64, true>(dq_accum, dQ, B, L, H, s)
+                : launch_post<64, false>(dq_accum, dQ, B, L, H, s);
+  return bf16 ? launch_post<128, true>(dq_accum, dQ, B, L, H, s)
+              : launch_post<128, false>(dq_accum, dQ, B, L, H, s);
 }
 
 fa_status run_bwd(const void* Q, const void* K, const void* V, const void* dO, const float* LSE,
                   const float* Delta, void* dQ, void* dK, void* dV, float* dq_accum,
                   int zero_accum, int B, int L, int H, int Hkv, int D, int causal, int dtype,
                   cudaStream_t s) {
-  const bool bf16 = dtype == FA_BF16;
-  if (D == 64)
-    return bf16 ? launch_bwd<64, true>(Q, K, V, dO, LSE, Delta, dQ, dK, dV, dq_accum, zero_accum,
-                                       B, L, H, Hkv, causal, s)
-                : launch_bwd<64, false>(Q, K, V, dO, LSE, Delta, dQ, dK, dV, dq_accum, zero_accum,
-                                        B, L, H, Hkv, causal, s);
-  return bf16 ? launch_bwd<128, true>(Q, K, V, dO, LSE, Delta, dQ, dK, dV, dq_accum, zero_accum, B,
-                                      L, H, Hkv, causal, s)
-              : launch_bwd<128, false>(Q, K, V, dO, LSE, Delta, dQ, dK, dV, dq_accum, zero_accum,
-                                       B, L, H, Hkv, causal, s);
+  fa_status st = run_bwd_main(Q, K, V, dO, LSE, Delta, dK, dV, dq_accum, zero_accum, B, L, H, Hkv,
+                              D, causal, dtype, s);
+  if (st != FA_OK) return st;
+  return run_bwd_post(dq_accum, dQ, B, L, H, D, dtype, s);
 }
 
 unsigned int bwd_read_error(cudaStream_t s) { return read_and_clear_error(s); }
