@@ -89,12 +89,15 @@ class ClockSampler:
              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, gpu_index):
+    def __init__(self, gpu_index, enabled=True):
         self.gpu = gpu_index
+        self.enabled = enabled
         self.proc = None
         self.tmp = None
 
     def start(self):
+        if not self.enabled:
+            return
         self.tmp = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
         try:
             self.proc = subprocess.Popen(
@@ -106,6 +109,8 @@ class ClockSampler:
         time.sleep(0.3)
 
     def stop(self):
+        if not self.enabled:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["not sampled"]}
         if self.proc is None:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
         self.proc.terminate()
@@ -278,7 +283,7 @@ def ours_arm(args):
 
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
     t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    sampler = ClockSampler(local)
+    sampler = ClockSampler(local, enabled=not args.no_clocks)
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
@@ -363,7 +368,7 @@ def ours_arm(args):
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         uq, uk, uv, udo = cpu_unit_inputs()
-        n, secs = time_oracle_units(uq, uk, uv, udo, causal, 8, args.cpu_budget)
+        n, secs = time_oracle_units(uq, uk, uv, udo, causal, 100000, args.cpu_budget)
         cpu = {"value": n * step_flops(1, 1, L, D, causal) / secs / 1e12, "unit": "TFLOP/s",
                "cores": blas_threads(), "kind": "oracle",
                "sample": f"{n} (batch, head) unit(s) of the workload, forward+backward in fp64 "
@@ -395,6 +400,8 @@ def main():
     ap.add_argument("--causal", action="store_true", help="causal masking (default: non-causal)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-clocks", action="store_true",
+                    help="skip the nvidia-smi clock sampler (for profiler runs)")
     ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle work")
     ap.add_argument("--batch", type=int, default=WORK["B"],
                     help="batch size (smaller values only for profiling captures)")

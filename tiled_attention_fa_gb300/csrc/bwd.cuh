@@ -10,20 +10,27 @@
 //      accumulator with atomics laid out to match the accumulator fragments;
 //   3. post-process: scale and convert the dQ accumulator back to BSHD.
 //
-// GB300 design of the main pass (320 threads, one CTA per SM, one K/V tile per CTA):
-//   warps 0-3  "softmax" warpgroup: thread r owns key row r of the K/V tile;
-//              P^T = exp2(S^T*c - LSE*log2e), dS^T = P^T o (dP^T - Delta);
-//              P^T goes to TMEM (A operand of dV += P^T dO), dS^T to swizzled
-//              smem (A operand of dK += dS^T Q and, read MN-major, of
-//              dQ = dS K); at the end it writes dK.
-//   warps 4-7  dQ drain: thread r owns query row r; reads the dQ tile from
-//              TMEM and adds it into the fp32 accumulator with 16-byte vector
-//              atomics; at the end it writes dV.
-//   warp  8    TMA producer: K_j, V_j once; then Q_i, dO_i (and LSE_i,
+// GB300 design of the main pass (512 threads, one CTA per SM, one K/V tile
+// of 128 keys per CTA):
+//   warps 0-3  compute warpgroup A: query columns 0-63 of every Q tile;
+//   warps 4-7  compute warpgroup B: query columns 64-127.  In both, thread r
+//              owns key row r (its TMEM lane) and forms
+//              P^T = exp2(S^T*c - LSE*log2e) and dS^T = P^T o (dP^T - Delta);
+//              P^T goes back to TMEM (A operand of dV += P^T dO), dS^T to a
+//              swizzled smem tile (A operand of dK += dS^T Q and, read
+//              MN-major, of dQ = dS K).  At the end A writes dK and B dV.
+//   warps 8-11 dQ drain: thread r owns query row r; reads the dQ tile from
+//              TMEM and adds it into the fp32 accumulator with 16-byte
+//              vector atomics.
+//   warp  12   TMA producer: K_j, V_j once; then Q_i, dO_i (and LSE_i,
 //              Delta_i) through a two-slot ring.
-//   warp  9    TMEM allocator and the single tcgen05.mma issuing thread.
-// dK and dV stay in TMEM for the whole CTA; for grouped-query attention the
-// CTA loops over every query head of its K/V head, so dK/dV need no atomics.
+//   warp  13   TMEM allocator and the single tcgen05.mma issuing thread.
+//   warps 14-15 idle.
+// The score and gradient MMAs are split by query halves, so the tensor core
+// computes half B's S^T/dP^T (and then half A's dV/dK products) while the
+// other warpgroup exponentiates.  dK and dV stay in TMEM for the whole CTA;
+// for grouped-query attention the CTA loops over every query head of its K/V
+// head, so dK/dV need no atomics.
 #pragma once
 
 #include <cuda_bf16.h>
@@ -58,24 +65,24 @@ struct BwdLayout {
   // Small region first (barriers, TMEM address, abort flag, LSE/Delta slots),
   // then the 1024-byte aligned operand tiles.
   static constexpr int B_KVFULL = 0, B_QFULL = 1, B_QEMPTY = 1 + STAGES, B_SFULL = 1 + 2 * STAGES,
-                       B_PFULL = B_SFULL + 1, B_DQFULL = B_PFULL + 1, B_DQEMPTY = B_DQFULL + 1,
+                       B_PFULL = B_SFULL + 2, B_DQFULL = B_PFULL + 2, B_DQEMPTY = B_DQFULL + 1,
                        B_DKVFULL = B_DQEMPTY + 1, B_DONE = B_DKVFULL + 1, NBAR = B_DONE + 1;
   static constexpr uint32_t BAR_OFF = 0;
-  static constexpr uint32_t MISC_OFF = BAR_OFF + NBAR * 8;          // tmem slot, abort flag
+  static constexpr uint32_t MISC_OFF = BAR_OFF + NBAR * 8;              // tmem slot, abort flag
   static constexpr uint32_t STAT_OFF = (MISC_OFF + 16 + 15) / 16 * 16;  // [STAGES][2][128] f32
   static constexpr uint32_t SMALL_END = STAT_OFF + STAGES * 2 * 128 * 4;
   static constexpr uint32_t TILE_BASE = (SMALL_END + 1023) / 1024 * 1024;
   static constexpr uint32_t K_OFF = TILE_BASE;
   static constexpr uint32_t V_OFF = K_OFF + TILE;
-  static constexpr uint32_t Q_OFF = V_OFF + TILE;                 // [STAGES] tiles
-  static constexpr uint32_t DO_OFF = Q_OFF + STAGES * TILE;       // [STAGES] tiles
-  static constexpr uint32_t DS_OFF = DO_OFF + STAGES * TILE;      // 2 chunks (128 keys x 128 queries)
+  static constexpr uint32_t Q_OFF = V_OFF + TILE;             // [STAGES] tiles
+  static constexpr uint32_t DO_OFF = Q_OFF + STAGES * TILE;   // [STAGES] tiles
+  static constexpr uint32_t DS_OFF = DO_OFF + STAGES * TILE;  // 2 chunks (128 keys x 128 queries)
   static constexpr uint32_t SMEM_ALLOC = DS_OFF + 2 * CHUNK;
   // TMEM columns
   static constexpr uint32_t TM_DK = 0, TM_DV = D, TM_S = 2 * D, TM_DP = 2 * D + 128;
   static constexpr uint32_t TM_DQ = (D == 128) ? TM_DP : (2 * D + 256);  // D=128: aliases dP^T
   static constexpr uint32_t TMEM_COLS = 512;
-  static constexpr int NTHREADS = 320;
+  static constexpr int NTHREADS = 512;
 };
 
 struct BwdItem {
@@ -105,15 +112,15 @@ __device__ __forceinline__ void bwd_tile(const BwdItem& it, const BwdParams& p, 
 }
 
 template <int D, bool BF16>
-__global__ void __launch_bounds__(320, 1)
+__global__ void __launch_bounds__(512, 1)
     fa_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
                   const BwdParams p) {
   using Ly = BwdLayout<D>;
   using T = typename std::conditional<BF16, __nv_bfloat16, __half>::type;
-  constexpr uint32_t IDESC_SS = idesc_f16(BF16, 128, 128, false, false);  // S^T, dP^T
-  constexpr uint32_t IDESC_KN = idesc_f16(BF16, 128, D, false, true);     // dV (A tmem), dK
-  constexpr uint32_t IDESC_MN = idesc_f16(BF16, 128, D, true, true);      // dQ
+  constexpr uint32_t IDESC_SS = idesc_f16(BF16, 128, 64, false, false);  // S^T, dP^T halves
+  constexpr uint32_t IDESC_KN = idesc_f16(BF16, 128, D, false, true);    // dV (A tmem), dK
+  constexpr uint32_t IDESC_MN = idesc_f16(BF16, 128, D, true, true);     // dQ
 
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   const uint32_t base = smem_u32(smem_raw);
@@ -136,8 +143,10 @@ __global__ void __launch_bounds__(320, 1)
       mbar_init(bar(Ly::B_QFULL + s), 32);
       mbar_init(bar(Ly::B_QEMPTY + s), 1);
     }
-    mbar_init(bar(Ly::B_SFULL), 1);
-    mbar_init(bar(Ly::B_PFULL), 128);
+    for (int c = 0; c < 2; ++c) {
+      mbar_init(bar(Ly::B_SFULL + c), 1);
+      mbar_init(bar(Ly::B_PFULL + c), 128);
+    }
     mbar_init(bar(Ly::B_DQFULL), 1);
     mbar_init(bar(Ly::B_DQEMPTY), 128);
     mbar_init(bar(Ly::B_DKVFULL), 1);
@@ -145,13 +154,13 @@ __global__ void __launch_bounds__(320, 1)
     ab->flag = 0;
     fence_barrier_init();
   }
-  if (warp == 8 && lane == 0) {
+  if (warp == 12 && lane == 0) {
     tma_prefetch_desc(&tmQ);
     tma_prefetch_desc(&tmK);
     tma_prefetch_desc(&tmV);
     tma_prefetch_desc(&tmdO);
   }
-  if (warp == 9) {
+  if (warp == 13) {
     tmem_alloc(base + Ly::MISC_OFF, Ly::TMEM_COLS);
     tmem_relinquish();
   }
@@ -161,7 +170,7 @@ __global__ void __launch_bounds__(320, 1)
   const uint32_t tmem = *tmem_slot;
   const int ntiles = it.ntiles;
 
-  if (warp == 8) {
+  if (warp == 12) {
     // ------------------------------------------------------------ producer (whole warp)
     bool ok = true;
     uint32_t issued[Ly::STAGES] = {0, 0};
@@ -212,7 +221,7 @@ __global__ void __launch_bounds__(320, 1)
       for (int s = 0; s < Ly::STAGES; ++s)
         if (issued[s] > 0) mbar_wait_drain(bar(Ly::B_QFULL + s), (issued[s] - 1) & 1);
     }
-  } else if (warp == 9) {
+  } else if (warp == 13) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       bool ok = mbar_wait(bar(Ly::B_KVFULL), 0, ab, err, 501);
@@ -224,43 +233,49 @@ __global__ void __launch_bounds__(320, 1)
         tc_fence_after();
         const uint32_t qa = base + Ly::Q_OFF + stage * Ly::TILE;
         const uint32_t doa = base + Ly::DO_OFF + stage * Ly::TILE;
-        // S^T = K_j Q_i^T  (keys x queries)
+        // Scores and score gradients, one 64-query half at a time:
+        //   S^T_c = K_j Q_c^T, dP^T_c = V_j dO_c^T  (keys x 64 queries)
 #pragma unroll
-        for (int k = 0; k < D / 16; ++k) {
-          const uint32_t off = (k >> 2) * Ly::CHUNK + (k & 3) * 32u;
-          mma_ss(tmem + Ly::TM_S, sdesc_sw128(ka + off, 16, 1024), sdesc_sw128(qa + off, 16, 1024),
-                 IDESC_SS, k > 0 ? 1u : 0u);
+        for (int c = 0; c < 2; ++c) {
+          const uint32_t roff = c * 8192u;  // query rows 64c.. start 64 rows into each chunk
+#pragma unroll
+          for (int k = 0; k < D / 16; ++k) {
+            const uint32_t off = (k >> 2) * Ly::CHUNK + (k & 3) * 32u;
+            mma_ss(tmem + Ly::TM_S + 64 * c, sdesc_sw128(ka + off, 16, 1024),
+                   sdesc_sw128(qa + off + roff, 16, 1024), IDESC_SS, k > 0 ? 1u : 0u);
+          }
+          if (D == 128 && c == 0 && n > 0) {  // dQ of the previous tile lives where dP^T goes
+            if (!mbar_wait(bar(Ly::B_DQEMPTY), (n - 1) & 1, ab, err, 503)) { ok = false; break; }
+            tc_fence_after();
+          }
+#pragma unroll
+          for (int k = 0; k < D / 16; ++k) {
+            const uint32_t off = (k >> 2) * Ly::CHUNK + (k & 3) * 32u;
+            mma_ss(tmem + Ly::TM_DP + 64 * c, sdesc_sw128(va + off, 16, 1024),
+                   sdesc_sw128(doa + off + roff, 16, 1024), IDESC_SS, k > 0 ? 1u : 0u);
+          }
+          tc_commit(bar(Ly::B_SFULL + c));
         }
-        if (D == 128 && n > 0) {  // dQ of the previous tile lives where dP^T goes
-          if (!mbar_wait(bar(Ly::B_DQEMPTY), (n - 1) & 1, ab, err, 503)) { ok = false; break; }
+        if (!ok) break;
+        // dV += P^T_c dO_c and dK += dS^T_c Q_c as each half's P^T / dS^T lands.
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          if (!mbar_wait(bar(Ly::B_PFULL + c), n & 1, ab, err, 504 + c)) { ok = false; break; }
           tc_fence_after();
-        }
-        // dP^T = V_j dO_i^T
 #pragma unroll
-        for (int k = 0; k < D / 16; ++k) {
-          const uint32_t off = (k >> 2) * Ly::CHUNK + (k & 3) * 32u;
-          mma_ss(tmem + Ly::TM_DP, sdesc_sw128(va + off, 16, 1024),
-                 sdesc_sw128(doa + off, 16, 1024), IDESC_SS, k > 0 ? 1u : 0u);
-        }
-        tc_commit(bar(Ly::B_SFULL));
-        if (!mbar_wait(bar(Ly::B_PFULL), n & 1, ab, err, 504)) { ok = false; break; }
-        tc_fence_after();
-        // dV += P^T dO_i   (P^T from TMEM, dO_i as an MN-major B operand)
+          for (int k = 0; k < 4; ++k)
+            mma_ts(tmem + Ly::TM_DV, tmem + Ly::TM_S + 64 * c + 8u * k,
+                   sdesc_sw128(doa + 2048u * (4 * c + k), Ly::CHUNK, 1024), IDESC_KN,
+                   (n > 0 || c > 0 || k > 0) ? 1u : 0u);
 #pragma unroll
-        for (int k = 0; k < 8; ++k)
-          mma_ts(tmem + Ly::TM_DV, tmem + Ly::TM_S + 8u * k,
-                 sdesc_sw128(doa + 2048u * k, Ly::CHUNK, 1024), IDESC_KN,
-                 (n > 0 || k > 0) ? 1u : 0u);
-        // dK += dS^T Q_i   (dS^T K-major in smem, Q_i MN-major)
-#pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          const uint32_t off = (k >> 2) * Ly::CHUNK + (k & 3) * 32u;
-          mma_ss(tmem + Ly::TM_DK, sdesc_sw128(dsa + off, 16, 1024),
-                 sdesc_sw128(qa + 2048u * k, Ly::CHUNK, 1024), IDESC_KN,
-                 (n > 0 || k > 0) ? 1u : 0u);
+          for (int k = 0; k < 4; ++k)
+            mma_ss(tmem + Ly::TM_DK, sdesc_sw128(dsa + c * Ly::CHUNK + 32u * k, 16, 1024),
+                   sdesc_sw128(qa + 2048u * (4 * c + k), Ly::CHUNK, 1024), IDESC_KN,
+                   (n > 0 || c > 0 || k > 0) ? 1u : 0u);
         }
+        if (!ok) break;
         if (D != 128 && n > 0) {
-          if (!mbar_wait(bar(Ly::B_DQEMPTY), (n - 1) & 1, ab, err, 505)) { ok = false; break; }
+          if (!mbar_wait(bar(Ly::B_DQEMPTY), (n - 1) & 1, ab, err, 506)) { ok = false; break; }
           tc_fence_after();
         }
         // dQ_i = dS K_j   (dS read MN-major from the dS^T tile, K_j MN-major)
@@ -279,80 +294,95 @@ __global__ void __launch_bounds__(320, 1)
       tc_commit(bar(Ly::B_DONE));
       mbar_wait_drain(bar(Ly::B_DONE), 0);
     }
-  } else if (warp < 4) {
-    // ------------------------------------------------------------ P^T / dS^T
+  } else if (warp < 8) {
+    // ------------------------------------------------------------ P^T / dS^T (one query half)
+    const int hc = warp >> 2;         // query half of this warpgroup
     const int r = threadIdx.x & 127;  // key row within the tile == TMEM lane
     const int kr = it.j * 128 + r;
     const uint32_t lane_off = ((warp & 3u) * 32u) << 16;
-    const uint32_t tS = tmem + lane_off + Ly::TM_S;
-    const uint32_t tP = tmem + lane_off + Ly::TM_DP;
+    const uint32_t tS = tmem + lane_off + Ly::TM_S + 64 * hc;
+    const uint32_t tP = tmem + lane_off + Ly::TM_DP + 64 * hc;
     const float sl2 = p.sl2;
-    uint8_t* ds_row = smem_raw + Ly::DS_OFF + r * 128;
+    uint8_t* ds_row = smem_raw + Ly::DS_OFF + hc * Ly::CHUNK + r * 128;
     bool ok = true;
     uint32_t stage = 0;
     for (int n = 0; n < ntiles; ++n) {
       int h, i;
       bwd_tile(it, p, n, h, i);
-      if (!mbar_wait_warp(bar(Ly::B_SFULL), n & 1, ab, err, 601)) { ok = false; break; }
+      if (!mbar_wait_warp(bar(Ly::B_SFULL + hc), n & 1, ab, err, 601)) { ok = false; break; }
       tc_fence_after();
-      const float* st = stats + stage * 256;
-      const int q0 = i * 128;
-      // query columns [lo, hi) of this tile are visible to key kr
-      int lo = 0, hi = min(128, p.L - q0);
+      const float* st = stats + stage * 256 + 64 * hc;
+      const int q0 = i * 128 + 64 * hc;
+      // query columns [lo, hi) of this half are visible to key kr
+      int lo = 0, hi = min(64, p.L - q0);
       if (kr >= p.L) hi = 0;
       if (p.causal) lo = max(0, kr - q0);
+      const bool full = (lo == 0 && hi == 64);
 #pragma unroll
-      for (int ch = 0; ch < 4; ++ch) {  // 32 query columns per chunk
+      for (int ch = 0; ch < 2; ++ch) {  // 32 query columns per chunk
         uint32_t s[32], dp[32];
         tmem_ld32(tS + 32 * ch, s);
         tmem_ld32(tP + 32 * ch, dp);
         tmem_ld_wait32(s);
         tmem_ld_wait32(dp);
         uint32_t pk[16], dk[16];
+        const float4* st4 = reinterpret_cast<const float4*>(st + 32 * ch);
+        const float4* dl4 = reinterpret_cast<const float4*>(st + 128 + 32 * ch);
 #pragma unroll
-        for (int u = 0; u < 16; ++u) {
-          float pv[2], dv[2];
+        for (int u4 = 0; u4 < 8; ++u4) {
+          const float4 l4 = st4[u4], d4 = dl4[u4];
+          const float lse[4] = {l4.x, l4.y, l4.z, l4.w};
+          const float dlt[4] = {d4.x, d4.y, d4.z, d4.w};
+          float pv[4], dv[4];
 #pragma unroll
-          for (int e = 0; e < 2; ++e) {
-            const int cl = 2 * u + e, c = 32 * ch + cl;
-            float pp = ex2(fmaf(__uint_as_float(s[cl]), sl2, -st[c]));
-            pp = (c >= lo && c < hi) ? pp : 0.f;
+          for (int e = 0; e < 4; ++e) {
+            const int cl = 4 * u4 + e;
+            float pp = ex2(fmaf(__uint_as_float(s[cl]), sl2, -lse[e]));
+            if (!full) {
+              const int c = 32 * ch + cl;
+              pp = (c >= lo && c < hi) ? pp : 0.f;
+            }
             pv[e] = pp;
-            dv[e] = pp * (__uint_as_float(dp[cl]) - st[128 + c]);
+            dv[e] = pp * (__uint_as_float(dp[cl]) - dlt[e]);
           }
-          pk[u] = pack2<T>(pv[0], pv[1]);
-          dk[u] = pack2<T>(dv[0], dv[1]);
+          pk[2 * u4] = pack2<T>(pv[0], pv[1]);
+          pk[2 * u4 + 1] = pack2<T>(pv[2], pv[3]);
+          dk[2 * u4] = pack2<T>(dv[0], dv[1]);
+          dk[2 * u4 + 1] = pack2<T>(dv[2], dv[3]);
         }
         // P^T columns (16-bit pairs) overwrite S^T columns already read.
         tmem_st16(tS + 16 * ch, pk);
-        // dS^T row r, queries 32*ch .. 32*ch+31: four swizzled 16-byte units.
-        uint8_t* chunk_row = ds_row + (ch >> 1) * Ly::CHUNK;
+        // dS^T row r, queries 64*hc + 32*ch .. +31: four swizzled 16-byte units.
 #pragma unroll
         for (int v = 0; v < 4; ++v) {
-          const int pos = ((ch & 1) * 4 + v) ^ (r & 7);
-          *reinterpret_cast<uint4*>(chunk_row + pos * 16) =
+          const int pos = (ch * 4 + v) ^ (r & 7);
+          *reinterpret_cast<uint4*>(ds_row + pos * 16) =
               make_uint4(dk[4 * v], dk[4 * v + 1], dk[4 * v + 2], dk[4 * v + 3]);
         }
       }
       tmem_st_wait();
       fence_proxy_async_smem();
       tc_fence_before();
-      mbar_arrive(bar(Ly::B_PFULL));
+      mbar_arrive(bar(Ly::B_PFULL + hc));
       if (++stage == Ly::STAGES) stage = 0;
     }
-    // dK epilogue: scale by 1/sqrt(D) and store row kr.
+    // Epilogue: warpgroup A writes dK (scaled by 1/sqrt(D)), B writes dV.
     if (ok && mbar_wait_warp(bar(Ly::B_DKVFULL), 0, ab, err, 602)) {
       tc_fence_after();
-      T* row = reinterpret_cast<T*>(p.dK) + ((static_cast<size_t>(it.b) * p.L + kr) * p.Hkv + it.hkv) * D;
+      void* dst_base = hc == 0 ? p.dK : p.dV;
+      const float sc = hc == 0 ? p.scale : 1.f;
+      const uint32_t tsrc = tmem + lane_off + (hc == 0 ? Ly::TM_DK : Ly::TM_DV);
+      T* row = reinterpret_cast<T*>(dst_base) +
+               ((static_cast<size_t>(it.b) * p.L + kr) * p.Hkv + it.hkv) * D;
 #pragma unroll
       for (int cc = 0; cc < D / 32; ++cc) {
         uint32_t o[32];
-        tmem_ld32(tmem + lane_off + Ly::TM_DK + 32 * cc, o);
+        tmem_ld32(tsrc + 32 * cc, o);
         tmem_ld_wait32(o);
         uint32_t pk[16];
 #pragma unroll
         for (int u = 0; u < 16; ++u)
-          pk[u] = pack2<T>(__uint_as_float(o[2 * u]) * p.scale, __uint_as_float(o[2 * u + 1]) * p.scale);
+          pk[u] = pack2<T>(__uint_as_float(o[2 * u]) * sc, __uint_as_float(o[2 * u + 1]) * sc);
         if (kr < p.L) {
           uint4* dst = reinterpret_cast<uint4*>(row + 32 * cc);
 #pragma unroll
@@ -361,16 +391,15 @@ __global__ void __launch_bounds__(320, 1)
         }
       }
     }
-  } else {
-    // ------------------------------------------------------------ dQ drain + dV epilogue
+  } else if (warp < 12) {
+    // ------------------------------------------------------------ dQ drain
     const int r = threadIdx.x & 127;  // query row within the Q tile == TMEM lane
     const uint32_t lane_off = ((warp & 3u) * 32u) << 16;
     const uint32_t tQ = tmem + lane_off + Ly::TM_DQ;
-    bool ok = true;
     for (int n = 0; n < ntiles; ++n) {
       int h, i;
       bwd_tile(it, p, n, h, i);
-      if (!mbar_wait_warp(bar(Ly::B_DQFULL), n & 1, ab, err, 701)) { ok = false; break; }
+      if (!mbar_wait_warp(bar(Ly::B_DQFULL), n & 1, ab, err, 701)) break;
       tc_fence_after();
       const int q = i * 128 + r;
       // accumulator layout [B, H, D/4, Lpad, 4]: a warp's 32 rows of one
@@ -382,6 +411,10 @@ __global__ void __launch_bounds__(320, 1)
         uint32_t g[32];
         tmem_ld32(tQ + 32 * cc, g);
         tmem_ld_wait32(g);
+        if (cc == D / 32 - 1) {  // every column of the tile is in registers now
+          tc_fence_before();
+          mbar_arrive(bar(Ly::B_DQEMPTY));
+        }
         if (q < p.L) {
 #pragma unroll
           for (int c4 = 0; c4 < 8; ++c4)
@@ -390,34 +423,12 @@ __global__ void __launch_bounds__(320, 1)
                                   __uint_as_float(g[4 * c4 + 2]), __uint_as_float(g[4 * c4 + 3])));
         }
       }
-      tc_fence_before();
-      mbar_arrive(bar(Ly::B_DQEMPTY));
-    }
-    if (ok && mbar_wait_warp(bar(Ly::B_DKVFULL), 0, ab, err, 702)) {
-      tc_fence_after();
-      const int kr = it.j * 128 + r;
-      T* row = reinterpret_cast<T*>(p.dV) + ((static_cast<size_t>(it.b) * p.L + kr) * p.Hkv + it.hkv) * D;
-#pragma unroll
-      for (int cc = 0; cc < D / 32; ++cc) {
-        uint32_t o[32];
-        tmem_ld32(tmem + lane_off + Ly::TM_DV + 32 * cc, o);
-        tmem_ld_wait32(o);
-        uint32_t pk[16];
-#pragma unroll
-        for (int u = 0; u < 16; ++u) pk[u] = pack2<T>(__uint_as_float(o[2 * u]), __uint_as_float(o[2 * u + 1]));
-        if (kr < p.L) {
-          uint4* dst = reinterpret_cast<uint4*>(row + 32 * cc);
-#pragma unroll
-          for (int u = 0; u < 4; ++u)
-            dst[u] = make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
-        }
-      }
     }
   }
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 9) {
+  if (warp == 13) {
     __syncwarp();
     tc_fence_after();
     tmem_dealloc(tmem, Ly::TMEM_COLS);

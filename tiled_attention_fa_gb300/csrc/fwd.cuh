@@ -9,13 +9,14 @@
 // product, and divides by l at the end.  Causal tiles past the diagonal are
 // never visited; K/V heads are shared by groups of query heads.
 //
-// GB300 design (not the page's): one persistent CTA per SM, 384 threads.
+// GB300 design (not the page's): one persistent CTA per SM, 320 threads.
 //   warps 0-3  softmax warpgroup for Q tile 0 (thread i owns row i)
 //   warps 4-7  softmax warpgroup for Q tile 1
 //   warp  8    TMA producer: Q pair, then K_j, V_j into a ring of smem slots
 //   warp  9    TMEM allocator and the single tcgen05.mma issuing thread
-//   warps 10-11 idle (they complete the third warpgroup so registers can be
-//              moved to the softmax warpgroups with setmaxnreg)
+// Registers are not re-balanced between warps (no setmaxnreg): a fixed split
+// depends on the launch allocation and would wait forever if a tool or
+// compiler changed it; the softmax instead stays within the uniform budget.
 // A work item is (batch, head, pair of 128-row Q tiles).  S_t = Q_t K_j^T and
 // O_t += P_t V_j accumulate in tensor memory; P_t overwrites S_t in TMEM as
 // 16-bit values and is read from there by the PV MMA.  While warpgroup 0
@@ -61,9 +62,7 @@ struct FwdLayout {
   static constexpr uint32_t SMEM_ALLOC = SMEM_USED + 1024;  // slack for 1024-byte alignment
   static constexpr uint32_t TM_S0 = 0, TM_S1 = 128, TM_O0 = 256, TM_O1 = 256 + D;
   static constexpr uint32_t TMEM_COLS = 512;
-  static constexpr int NTHREADS = 384;
-  // setmaxnreg split: 2 x 128 x 208 + 128 x 88 = 384 x 168 (the launch allocation)
-  static constexpr uint32_t REGS_SOFTMAX = 208, REGS_OTHER = 88;
+  static constexpr int NTHREADS = 320;
 };
 
 struct FwdItem {
@@ -103,7 +102,7 @@ __device__ __forceinline__ uint32_t pack2<__nv_bfloat16>(float lo, float hi) {
 }
 
 template <int D, bool BF16>
-__global__ void __launch_bounds__(384, 1)
+__global__ void __launch_bounds__(320, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const FwdParams p) {
   using Ly = FwdLayout<D>;
@@ -154,7 +153,6 @@ __global__ void __launch_bounds__(384, 1)
   const uint32_t tmem = *tmem_slot;
 
   if (warp >= 8) {
-    regs_dec<Ly::REGS_OTHER>();
   if (warp == 8) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
@@ -295,10 +293,7 @@ __global__ void __launch_bounds__(384, 1)
       mbar_wait_drain(bar(Ly::B_DONE), 0);
     }
   }
-    __syncwarp();
-    regs_inc<168>();
   } else {
-    regs_inc<Ly::REGS_SOFTMAX>();
     // ------------------------------------------------------------ softmax
     const int t = warp >> 2;                       // Q tile of this warpgroup
     const int r = threadIdx.x & 127;               // row within the tile == TMEM lane
@@ -343,42 +338,45 @@ __global__ void __launch_bounds__(384, 1)
           for (int c = 0; c < 128; ++c) mx = fmaxf(mx, __uint_as_float(sr[c]));
         }
         const float m_new = fmaxf(m, mx);
+        float alpha = 1.f;
+        bool rescale = false;
         if (j == 0) {
           m = m_new;
-        } else {
-          const bool grow = (m_new - m) * sl2 > 8.0f;
-          if (__any_sync(0xffffffffu, grow)) {
-            // Rescale this warp's O rows (PV of the previous tile has completed:
-            // the commit that signalled S of this tile covers it).
-            const float alpha = ex2((m - m_new) * sl2);
-            m = m_new;
-            l *= alpha;
-#pragma unroll
-            for (int cc = 0; cc < D / 32; ++cc) {
-              uint32_t o[32];
-              tmem_ld32(tO + 32 * cc, o);
-              tmem_ld_wait32(o);
-#pragma unroll
-              for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-              tmem_st32(tO + 32 * cc, o);
-            }
-          }
+        } else if (__any_sync(0xffffffffu, (m_new - m) * sl2 > 8.0f)) {
+          // The running max grew by more than 2^8 somewhere in this warp:
+          // rescale this warp's rows (others get alpha = 1).
+          alpha = ex2((m - m_new) * sl2);
+          m = m_new;
+          rescale = true;
         }
         const float mb = m * sl2;
         float rs = 0.f;
 #pragma unroll
-        for (int h2 = 0; h2 < 2; ++h2) {
-          uint32_t pk[32];
+        for (int q4 = 0; q4 < 4; ++q4) {
+          uint32_t pk[16];
 #pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            const float p0 = ex2(fmaf(__uint_as_float(sr[64 * h2 + 2 * i]), sl2, -mb));
-            const float p1 = ex2(fmaf(__uint_as_float(sr[64 * h2 + 2 * i + 1]), sl2, -mb));
+          for (int i = 0; i < 16; ++i) {
+            const float p0 = ex2(fmaf(__uint_as_float(sr[32 * q4 + 2 * i]), sl2, -mb));
+            const float p1 = ex2(fmaf(__uint_as_float(sr[32 * q4 + 2 * i + 1]), sl2, -mb));
             rs += p0 + p1;
             pk[i] = pack2<T>(p0, p1);
           }
-          tmem_st32(tS + 32 * h2, pk);
+          tmem_st16(tS + 16 * q4, pk);
         }
-        l += rs;
+        if (rescale) {
+          // O of this row scaled by alpha.  PV of the previous tile has
+          // completed: the commit that signalled this tile's S covers it.
+#pragma unroll
+          for (int cc = 0; cc < D / 32; ++cc) {
+            uint32_t o[32];
+            tmem_ld32(tO + 32 * cc, o);
+            tmem_ld_wait32(o);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+            tmem_st32(tO + 32 * cc, o);
+          }
+        }
+        l = l * alpha + rs;
         tmem_st_wait();
         tc_fence_before();
         mbar_arrive(bar(Ly::B_PFULL + t));
@@ -412,8 +410,6 @@ __global__ void __launch_bounds__(384, 1)
       tc_fence_before();
       mbar_arrive(bar(Ly::B_OEMPTY + t));
     }
-    __syncwarp();
-    regs_dec<168>();
   }
 
   tc_fence_before();
