@@ -66,7 +66,7 @@ struct BwdLayout {
   // then the 1024-byte aligned operand tiles.
   static constexpr int B_KVFULL = 0, B_QFULL = 1, B_QEMPTY = 1 + STAGES, B_SFULL = 1 + 2 * STAGES,
                        B_PFULL = B_SFULL + 2, B_DQFULL = B_PFULL + 2, B_DQEMPTY = B_DQFULL + 1,
-                       B_DKVFULL = B_DQEMPTY + 1, B_DONE = B_DKVFULL + 1, NBAR = B_DONE + 1;
+                       B_DKVFULL = B_DQEMPTY + 2, B_DONE = B_DKVFULL + 1, NBAR = B_DONE + 1;
   static constexpr uint32_t BAR_OFF = 0;
   static constexpr uint32_t MISC_OFF = BAR_OFF + NBAR * 8;              // tmem slot, abort flag
   static constexpr uint32_t STAT_OFF = (MISC_OFF + 16 + 15) / 16 * 16;  // [STAGES][2][128] f32
@@ -80,7 +80,14 @@ struct BwdLayout {
   static constexpr uint32_t SMEM_ALLOC = DS_OFF + 2 * CHUNK;
   // TMEM columns
   static constexpr uint32_t TM_DK = 0, TM_DV = D, TM_S = 2 * D, TM_DP = 2 * D + 128;
-  static constexpr uint32_t TM_DQ = (D == 128) ? TM_DP : (2 * D + 256);  // D=128: aliases dP^T
+  // The dQ tile is produced as D/64 halves of 64 columns.  D=64: its own
+  // columns.  D=128: half 0 sits in the S^T columns of query half B and half
+  // 1 in the dP^T columns of query half B, so the next tile's half-A work
+  // never waits for the dQ drain; each half is released on its own barrier.
+  static constexpr int NDQ = D / 64;
+  __host__ __device__ static constexpr uint32_t tm_dq(int h) {
+    return D == 128 ? (h == 0 ? TM_S + 64 : TM_DP + 64) : (2 * D + 256);
+  }
   static constexpr uint32_t TMEM_COLS = 512;
   static constexpr int NTHREADS = 512;
 };
@@ -120,7 +127,7 @@ __global__ void __launch_bounds__(512, 1)
   using T = typename std::conditional<BF16, __nv_bfloat16, __half>::type;
   constexpr uint32_t IDESC_SS = idesc_f16(BF16, 128, 64, false, false);  // S^T, dP^T halves
   constexpr uint32_t IDESC_KN = idesc_f16(BF16, 128, D, false, true);    // dV (A tmem), dK
-  constexpr uint32_t IDESC_MN = idesc_f16(BF16, 128, D, true, true);     // dQ
+  constexpr uint32_t IDESC_MN = idesc_f16(BF16, 128, 64, true, true);    // dQ halves
 
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   const uint32_t base = smem_u32(smem_raw);
@@ -149,6 +156,7 @@ __global__ void __launch_bounds__(512, 1)
     }
     mbar_init(bar(Ly::B_DQFULL), 1);
     mbar_init(bar(Ly::B_DQEMPTY), 128);
+    mbar_init(bar(Ly::B_DQEMPTY + 1), 128);
     mbar_init(bar(Ly::B_DKVFULL), 1);
     mbar_init(bar(Ly::B_DONE), 1);
     ab->flag = 0;
@@ -238,14 +246,19 @@ __global__ void __launch_bounds__(512, 1)
 #pragma unroll
         for (int c = 0; c < 2; ++c) {
           const uint32_t roff = c * 8192u;  // query rows 64c.. start 64 rows into each chunk
+          // D=128: half B's S^T / dP^T columns held the previous tile's dQ halves.
+          if (D == 128 && c == 1 && n > 0) {
+            if (!mbar_wait(bar(Ly::B_DQEMPTY), (n - 1) & 1, ab, err, 503)) { ok = false; break; }
+            tc_fence_after();
+          }
 #pragma unroll
           for (int k = 0; k < D / 16; ++k) {
             const uint32_t off = (k >> 2) * Ly::CHUNK + (k & 3) * 32u;
             mma_ss(tmem + Ly::TM_S + 64 * c, sdesc_sw128(ka + off, 16, 1024),
                    sdesc_sw128(qa + off + roff, 16, 1024), IDESC_SS, k > 0 ? 1u : 0u);
           }
-          if (D == 128 && c == 0 && n > 0) {  // dQ of the previous tile lives where dP^T goes
-            if (!mbar_wait(bar(Ly::B_DQEMPTY), (n - 1) & 1, ab, err, 503)) { ok = false; break; }
+          if (D == 128 && c == 1 && n > 0) {
+            if (!mbar_wait(bar(Ly::B_DQEMPTY + 1), (n - 1) & 1, ab, err, 507)) { ok = false; break; }
             tc_fence_after();
           }
 #pragma unroll
@@ -278,11 +291,15 @@ __global__ void __launch_bounds__(512, 1)
           if (!mbar_wait(bar(Ly::B_DQEMPTY), (n - 1) & 1, ab, err, 506)) { ok = false; break; }
           tc_fence_after();
         }
-        // dQ_i = dS K_j   (dS read MN-major from the dS^T tile, K_j MN-major)
+        // dQ_i = dS K_j in 64-column halves (dS read MN-major from the dS^T
+        // tile, K_j MN-major).
 #pragma unroll
-        for (int k = 0; k < 8; ++k)
-          mma_ss(tmem + Ly::TM_DQ, sdesc_sw128(dsa + 2048u * k, Ly::CHUNK, 1024),
-                 sdesc_sw128(ka + 2048u * k, Ly::CHUNK, 1024), IDESC_MN, k > 0 ? 1u : 0u);
+        for (int hq = 0; hq < Ly::NDQ; ++hq)
+#pragma unroll
+          for (int k = 0; k < 8; ++k)
+            mma_ss(tmem + Ly::tm_dq(hq), sdesc_sw128(dsa + 2048u * k, Ly::CHUNK, 1024),
+                   sdesc_sw128(ka + hq * Ly::CHUNK + 2048u * k, Ly::CHUNK, 1024), IDESC_MN,
+                   k > 0 ? 1u : 0u);
         tc_commit(bar(Ly::B_DQFULL));
         tc_commit(bar(Ly::B_QEMPTY + stage));
         if (++stage == Ly::STAGES) {
@@ -395,7 +412,6 @@ __global__ void __launch_bounds__(512, 1)
     // ------------------------------------------------------------ dQ drain
     const int r = threadIdx.x & 127;  // query row within the Q tile == TMEM lane
     const uint32_t lane_off = ((warp & 3u) * 32u) << 16;
-    const uint32_t tQ = tmem + lane_off + Ly::TM_DQ;
     for (int n = 0; n < ntiles; ++n) {
       int h, i;
       bwd_tile(it, p, n, h, i);
@@ -407,18 +423,19 @@ __global__ void __launch_bounds__(512, 1)
       float4* acc = reinterpret_cast<float4*>(p.dq_accum) +
                     (static_cast<size_t>(it.b) * p.H + h) * (D / 4) * p.Lpad + q;
 #pragma unroll
-      for (int cc = 0; cc < D / 32; ++cc) {
-        uint32_t g[32];
-        tmem_ld32(tQ + 32 * cc, g);
+      for (int hq = 0; hq < Ly::NDQ; ++hq) {
+        uint32_t g[64];
+        tmem_ld32(tmem + lane_off + Ly::tm_dq(hq), g);
+        tmem_ld32(tmem + lane_off + Ly::tm_dq(hq) + 32, g + 32);
         tmem_ld_wait32(g);
-        if (cc == D / 32 - 1) {  // every column of the tile is in registers now
-          tc_fence_before();
-          mbar_arrive(bar(Ly::B_DQEMPTY));
-        }
+        tmem_ld_wait32(g + 32);
+        // This half is in registers: release its columns before the atomics.
+        tc_fence_before();
+        mbar_arrive(bar(Ly::B_DQEMPTY + hq));
         if (q < p.L) {
 #pragma unroll
-          for (int c4 = 0; c4 < 8; ++c4)
-            atomicAdd(acc + static_cast<size_t>(8 * cc + c4) * p.Lpad,
+          for (int c4 = 0; c4 < 16; ++c4)
+            atomicAdd(acc + static_cast<size_t>(16 * hq + c4) * p.Lpad,
                       make_float4(__uint_as_float(g[4 * c4]), __uint_as_float(g[4 * c4 + 1]),
                                   __uint_as_float(g[4 * c4 + 2]), __uint_as_float(g[4 * c4 + 3])));
         }
