@@ -34,7 +34,8 @@ typedef enum {
   FA_ERR_INVALID_ARG = 1,    /* null/misaligned pointer, bad size, H % Hkv != 0 */
   FA_ERR_UNSUPPORTED = 2,    /* D or dtype outside the supported set */
   FA_ERR_CUDA = 3,           /* a CUDA runtime call or kernel launch failed */
-  FA_ERR_DEVICE_TIMEOUT = 4  /* a kernel gave up a bounded wait (see fa_check_device_error) */
+  FA_ERR_DEVICE_TIMEOUT = 4, /* a kernel gave up a bounded wait (see fa_check_device_error) */
+  FA_ERR_SCRATCH_TOO_SMALL = 5 /* fa_bwd_noalloc: the problem needs more than its fixed scratch */
 } fa_status;
 
 typedef enum { FA_F16 = 0, FA_BF16 = 1 } fa_dtype;
@@ -106,6 +107,34 @@ fa_status fa_bwd_main(const void* Q, const void* K, const void* V, const void* d
                       void* stream);
 fa_status fa_bwd_postprocess(const float* dq_accum, void* dQ, int B, int L, int H, int D,
                              int dtype, void* stream);
+
+/*
+ * fa_bwd for callers that cannot allocate device memory at call time: a
+ * plugin running inside a host application that owns all GPU memory through
+ * its own pool and hands out no allocator, or a serving path that must not
+ * allocate once it has started.  This is a library facility; the pages have
+ * no counterpart.
+ * Same arguments and results as fa_bwd, minus the workspace: the fp32 dQ
+ * accumulator lives in a fixed device array of FA_NOALLOC_SCRATCH_BYTES that
+ * the library's module holds on every GPU that loads it, until exit.  The
+ * call allocates nothing (no cudaMalloc, cudaFree or allocating library
+ * routine); it clears the part of the array it uses, then runs the backward.
+ * Limits and rules:
+ *   - B * H * ceil(L/128)*128 * D * 4 bytes must not exceed
+ *     FA_NOALLOC_SCRATCH_BYTES (64 MiB, e.g. B=1, H=32, L=4096, D=128);
+ *     larger problems return FA_ERR_SCRATCH_TOO_SMALL and launch nothing.
+ *   - Every call on a device shares the one array: calls whose work overlaps
+ *     on the GPU (other streams, other host threads) race and corrupt each
+ *     other's dQ.  Serialise them.
+ *   - The first call on each device looks up the array's device address
+ *     (with that device current); make that first call before any stream
+ *     capture on the device.
+ */
+#define FA_NOALLOC_SCRATCH_BYTES ((size_t)64 << 20)
+fa_status fa_bwd_noalloc(const void* Q, const void* K, const void* V, const void* O,
+                         const void* dO, const float* LSE, const float* Delta, void* dQ,
+                         void* dK, void* dV, int B, int L, int H, int Hkv, int D, int causal,
+                         int dtype, void* stream);
 
 /*
  * Synchronise `stream` and report whether any kernel of this library gave up

@@ -15,6 +15,8 @@ LIB_PATH = os.path.join(HERE, "libfa_gb300.so")
 HEADER = os.path.join(os.path.dirname(HERE), "include", "fa.h")
 
 FA_OK, FA_ERR_INVALID_ARG, FA_ERR_UNSUPPORTED, FA_ERR_CUDA, FA_ERR_DEVICE_TIMEOUT = range(5)
+FA_ERR_SCRATCH_TOO_SMALL = 5
+FA_NOALLOC_SCRATCH_BYTES = 64 << 20
 FA_F16, FA_BF16 = 0, 1
 
 _lib = None
@@ -28,6 +30,7 @@ _SIGS = {
     "fa_bwd": ([_vp] * 11 + [_i] * 8 + [_vp], _i),
     "fa_bwd_main": ([_vp] * 9 + [_i] * 8 + [_vp], _i),
     "fa_bwd_postprocess": ([_vp, _vp] + [_i] * 5 + [_vp], _i),
+    "fa_bwd_noalloc": ([_vp] * 10 + [_i] * 7 + [_vp], _i),
     "fa_check_device_error": ([_vp], _i),
     "fa_last_error_site": ([], ctypes.c_uint),
     "fa_status_string": ([_i], ctypes.c_char_p),

@@ -90,6 +90,20 @@ fa_status fa_bwd_postprocess(const float* dq_accum, void* dQ, int B, int L, int 
   return fa::run_bwd_post(dq_accum, dQ, B, L, H, D, dtype, static_cast<cudaStream_t>(stream));
 }
 
+fa_status fa_bwd_noalloc(const void* Q, const void* K, const void* V, const void* O,
+                         const void* dO, const float* LSE, const float* Delta, void* dQ,
+                         void* dK, void* dV, int B, int L, int H, int Hkv, int D, int causal,
+                         int dtype, void* stream) {
+  (void)O;
+  fa_status st = check_shape(B, L, H, Hkv, D, dtype);
+  if (st != FA_OK) return st;
+  if (!ptr_ok(Q) || !ptr_ok(K) || !ptr_ok(V) || !ptr_ok(dO) || !ptr_ok(LSE) || !ptr_ok(Delta) ||
+      !ptr_ok(dQ) || !ptr_ok(dK) || !ptr_ok(dV))
+    return FA_ERR_INVALID_ARG;
+  return fa::run_bwd_noalloc(Q, K, V, dO, LSE, Delta, dQ, dK, dV, B, L, H, Hkv, D, causal, dtype,
+                             static_cast<cudaStream_t>(stream));
+}
+
 fa_status fa_check_device_error(void* stream) {
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const unsigned int a = fa::fwd_read_error(s);
@@ -111,6 +125,8 @@ const char* fa_status_string(fa_status s) {
     case FA_ERR_UNSUPPORTED: return "unsupported head dimension or dtype";
     case FA_ERR_CUDA: return "CUDA runtime or launch error";
     case FA_ERR_DEVICE_TIMEOUT: return "a kernel gave up a bounded wait";
+    case FA_ERR_SCRATCH_TOO_SMALL:
+      return "problem needs more dQ scratch than fa_bwd_noalloc's fixed array holds";
   }
   return "unknown status";
 }

@@ -1,4 +1,5 @@
 // Host launchers of the backward kernels (preprocess, main pass, dQ post-process).
+#include <mutex>
 #include <type_traits>
 
 #include "bwd.cuh"
@@ -121,5 +122,49 @@ fa_status run_bwd(const void* Q, const void* K, const void* V, const void* dO, c
 }
 
 unsigned int bwd_read_error(cudaStream_t s) { return read_and_clear_error(s); }
+
+// ---------------------------------------------------------------- no-allocation variant
+// Scratch for fa_bwd_noalloc's fp32 dQ accumulator.  It is part of this
+// module's device image, so every GPU that loads the library holds these
+// FA_NOALLOC_SCRATCH_BYTES until the process exits; all calls share it.
+static __device__ __align__(256) float g_noalloc_dq_accum[FA_NOALLOC_SCRATCH_BYTES / sizeof(float)];
+
+namespace {
+constexpr int kMaxDevices = 64;
+std::mutex g_noalloc_mu;
+float* g_noalloc_ptr[kMaxDevices] = {};
+
+// Device address of the scratch array on the current device.  In host code
+// the array's name is only a host-side stand-in, so the address is looked up
+// once per device (with that device current) and cached.
+fa_status noalloc_scratch(float** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return FA_ERR_CUDA;
+  if (dev < 0 || dev >= kMaxDevices) return FA_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  if (g_noalloc_ptr[dev] == nullptr) {
+    void* ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, g_noalloc_dq_accum) != cudaSuccess || ptr == nullptr)
+      return FA_ERR_CUDA;
+    g_noalloc_ptr[dev] = static_cast<float*>(ptr);
+  }
+  *out = g_noalloc_ptr[dev];
+  return FA_OK;
+}
+}  // namespace
+
+fa_status run_bwd_noalloc(const void* Q, const void* K, const void* V, const void* dO,
+                          const float* LSE, const float* Delta, void* dQ, void* dK, void* dV,
+                          int B, int L, int H, int Hkv, int D, int causal, int dtype,
+                          cudaStream_t s) {
+  const size_t need = static_cast<size_t>(B) * H * padded_len(L) * D * sizeof(float);
+  if (need > FA_NOALLOC_SCRATCH_BYTES) return FA_ERR_SCRATCH_TOO_SMALL;
+  float* acc = nullptr;
+  fa_status st = noalloc_scratch(&acc);
+  if (st != FA_OK) return st;
+  // The array keeps the previous call's sums: clear the part this call uses.
+  if (cudaMemsetAsync(acc, 0, need, s) != cudaSuccess) return FA_ERR_CUDA;
+  return run_bwd(Q, K, V, dO, LSE, Delta, dQ, dK, dV, acc, 0, B, L, H, Hkv, D, causal, dtype, s);
+}
 
 }  // namespace fa

@@ -24,6 +24,10 @@ fa_status run_bwd_main(const void* Q, const void* K, const void* V, const void* 
 fa_status run_bwd_post(const float* dq_accum, void* dQ, int B, int L, int H, int D, int dtype,
                        cudaStream_t s);
 unsigned int bwd_read_error(cudaStream_t s);
+fa_status run_bwd_noalloc(const void* Q, const void* K, const void* V, const void* dO,
+                          const float* LSE, const float* Delta, void* dQ, void* dK, void* dV,
+                          int B, int L, int H, int Hkv, int D, int causal, int dtype,
+                          cudaStream_t s);
 
 inline int padded_len(int L) { return (L + 127) / 128 * 128; }
 
