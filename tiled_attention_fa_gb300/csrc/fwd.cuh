@@ -88,6 +88,16 @@ __device__ __forceinline__ FwdItem fwd_decode(int item, const FwdParams& p) {
   return it;
 }
 
+// Items are handed out in rounds of gridDim.x, alternating direction each
+// round (CTA c takes position c, then G-1-c, ...).  Within a head the pairs
+// run longest-first, so under causal masking every CTA gets a mix of long
+// and short items; consecutive items still share a head's K/V in L2.
+__device__ __forceinline__ int fwd_item_of(int round) {
+  const int G = static_cast<int>(gridDim.x);
+  const int pos = (round & 1) ? (G - 1 - static_cast<int>(blockIdx.x)) : static_cast<int>(blockIdx.x);
+  return round * G + pos;
+}
+
 template <typename T>
 __device__ __forceinline__ uint32_t pack2(float lo, float hi);
 template <>
@@ -161,7 +171,9 @@ __global__ void __launch_bounds__(320, 1)
       for (int s = 0; s < Ly::STAGES; ++s) issued[s] = 0;
       const uint64_t keep = policy_evict_last();
       bool ok = true;
-      for (int item = blockIdx.x; ok && item < p.n_items; item += gridDim.x) {
+      for (int round = 0; ok && round * static_cast<int>(gridDim.x) < p.n_items; ++round) {
+        const int item = fwd_item_of(round);
+        if (item >= p.n_items) continue;
         const FwdItem it = fwd_decode(item, p);
         if (q_uses > 0 && !mbar_wait(bar(Ly::B_QEMPTY), (q_uses - 1) & 1, ab, err, 101)) {
           ok = false;
@@ -238,7 +250,9 @@ __global__ void __launch_bounds__(320, 1)
         return true;
       };
 
-      for (int item = blockIdx.x; ok && item < p.n_items; item += gridDim.x) {
+      for (int round = 0; ok && round * static_cast<int>(gridDim.x) < p.n_items; ++round) {
+        const int item = fwd_item_of(round);
+        if (item >= p.n_items) continue;
         const FwdItem it = fwd_decode(item, p);
         const int nmax = max(it.n[0], it.n[1]);
         if (!mbar_wait(bar(Ly::B_QFULL), q_cnt & 1, ab, err, 201)) { ok = false; break; }
@@ -303,7 +317,9 @@ __global__ void __launch_bounds__(320, 1)
     const float sl2 = p.sl2;
     uint32_t s_cnt = 0, o_cnt = 0;
     bool ok = true;
-    for (int item = blockIdx.x; ok && item < p.n_items; item += gridDim.x) {
+    for (int round = 0; ok && round * static_cast<int>(gridDim.x) < p.n_items; ++round) {
+        const int item = fwd_item_of(round);
+        if (item >= p.n_items) continue;
       const FwdItem it = fwd_decode(item, p);
       const int n = it.n[t];
       if (n == 0) continue;
