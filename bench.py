@@ -189,10 +189,8 @@ def cpu_unit_inputs(seed=0):
 # --------------------------------------------------------------------- arms
 
 def dist_setup():
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    rank = int(os.environ.get("RANK", "0"))
-    local = int(os.environ.get("LOCAL_RANK", "0"))
-    return world, rank, local
+    from tiled_attention_fa_gb300.replicas import dist_env
+    return dist_env()
 
 
 def reference_arm(args):
@@ -233,21 +231,19 @@ def config_dict(args, world):
 
 def ours_arm(args):
     import torch
-    import torch.distributed as dist
     import tiled_attention_fa_gb300 as fa
-    from tiled_attention_fa_gb300 import _lib
+    from tiled_attention_fa_gb300 import _lib, replicas
 
     world, rank, local = dist_setup()
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
-    if world > 1:
-        dist.init_process_group("nccl", device_id=dev)
+    replicas.init("nccl", dev)
     _lib.load()  # fails loudly without the built library
 
     B, L, H, Hkv, D = WORK["B"], WORK["L"], WORK["H"], WORK["Hkv"], WORK["D"]
     causal = bool(args.causal)
     dt = torch.float16
-    g = torch.Generator(device=dev).manual_seed(1234 + rank)
+    g = torch.Generator(device=dev).manual_seed(replicas.replica_seed(1234, rank))
     q = torch.randn(B, L, H, D, device=dev, dtype=dt, generator=g)
     k = torch.randn(B, L, Hkv, D, device=dev, dtype=dt, generator=g)
     v = torch.randn(B, L, Hkv, D, device=dev, dtype=dt, generator=g)
@@ -284,8 +280,7 @@ def ours_arm(args):
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
     t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     sampler = ClockSampler(local, enabled=not args.no_clocks)
-    if world > 1:
-        dist.barrier()
+    replicas.barrier()
     torch.cuda.synchronize()
     sampler.start()
     t_start.record(stream)
@@ -293,15 +288,10 @@ def ours_arm(args):
         step(evs[i])
     t_end.record(stream)
     torch.cuda.synchronize()
-    if world > 1:
-        dist.barrier()
+    replicas.barrier()
     clocks = sampler.stop()
     fa.check_device_error()
-    ms = t_start.elapsed_time(t_end)
-    if world > 1:
-        t = torch.tensor([ms], device=dev, dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = replicas.max_over_ranks(t_start.elapsed_time(t_end), dev)
     ms_per_step = ms / args.steps
 
     names = ["fa_fwd_kernel", "fa_bwd_prep_kernel", "fa_bwd_kernel", "fa_dq_convert_kernel"]
@@ -335,7 +325,7 @@ def ours_arm(args):
                 "frac": ach / hbm, "peak_source": f"{src} copy bandwidth"}
     roof["traffic"] = recorded_traffic(dom)
 
-    value = world * step_flops(B, H, L, D, causal) / (ms_per_step * 1e-3) / 1e12
+    value = replicas.aggregate_rate(step_flops(B, H, L, D, causal), world, ms_per_step * 1e-3) / 1e12
 
     # ---- end to end through the public API with host buffers
     e2e = None
@@ -346,20 +336,15 @@ def ours_arm(args):
         torch.cuda.synchronize()
         n_e2e = max(3, min(args.steps, 10))
         s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        if world > 1:
-            dist.barrier()
+        replicas.barrier()
         torch.cuda.synchronize()
         s0.record(stream)
         for _ in range(n_e2e):
             runner.run(hq, hk, hv, hdo, stream=stream)
         s1.record(stream)
         torch.cuda.synchronize()
-        ems = s0.elapsed_time(s1) / n_e2e
-        if world > 1:
-            t = torch.tensor([ems], device=dev, dtype=torch.float64)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            ems = float(t.item())
-        e2e = {"value": world * step_flops(B, H, L, D, causal) / (ems * 1e-3) / 1e12,
+        ems = replicas.max_over_ranks(s0.elapsed_time(s1) / n_e2e, dev)
+        e2e = {"value": replicas.aggregate_rate(step_flops(B, H, L, D, causal), world, ems * 1e-3) / 1e12,
                "unit": "TFLOP/s", "h2d_bytes_per_step": runner.h2d_bytes(),
                "d2h_bytes_per_step": runner.d2h_bytes(), "ms_per_step": ems, "steps": n_e2e}
         del runner
@@ -387,6 +372,7 @@ def ours_arm(args):
         }
         print(json.dumps(out), flush=True)
     if world > 1:
+        import torch.distributed as dist
         dist.destroy_process_group()
     return 0
 

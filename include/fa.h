@@ -144,6 +144,17 @@ fa_status fa_bwd_noalloc(const void* Q, const void* K, const void* V, const void
  */
 fa_status fa_check_device_error(void* stream);
 
+/*
+ * Exercise the bounded-wait failure path without any fault: launches one
+ * thread that waits on an mbarrier nothing ever completes.  After
+ * `limit_ns` (clamped to 1 ms .. 1 s) the wait gives up, records site 900 in
+ * the device error word and the kernel returns; the next
+ * fa_check_device_error on the stream then returns FA_ERR_DEVICE_TIMEOUT and
+ * the CUDA context stays usable.  A library facility with no counterpart on
+ * the pages.
+ */
+fa_status fa_selftest_bounded_wait(unsigned long long limit_ns, void* stream);
+
 /* Site id recorded by the last FA_ERR_DEVICE_TIMEOUT (0 if none). */
 unsigned int fa_last_error_site(void);
 

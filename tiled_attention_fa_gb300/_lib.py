@@ -33,6 +33,7 @@ _SIGS = {
     "fa_bwd_noalloc": ([_vp] * 10 + [_i] * 7 + [_vp], _i),
     "fa_check_device_error": ([_vp], _i),
     "fa_last_error_site": ([], ctypes.c_uint),
+    "fa_selftest_bounded_wait": ([ctypes.c_ulonglong, _vp], _i),
     "fa_status_string": ([_i], ctypes.c_char_p),
     "fa_version": ([], ctypes.c_char_p),
 }

@@ -116,6 +116,12 @@ fa_status fa_check_device_error(void* stream) {
   return FA_OK;
 }
 
+fa_status fa_selftest_bounded_wait(unsigned long long limit_ns, void* stream) {
+  if (limit_ns < 1000000ull) limit_ns = 1000000ull;
+  if (limit_ns > 1000000000ull) limit_ns = 1000000000ull;
+  return fa::run_selftest_wait(limit_ns, static_cast<cudaStream_t>(stream));
+}
+
 unsigned int fa_last_error_site(void) { return g_last_site; }
 
 const char* fa_status_string(fa_status s) {

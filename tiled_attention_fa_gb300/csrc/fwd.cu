@@ -49,4 +49,23 @@ fa_status run_fwd(const void* Q, const void* K, const void* V, void* O, float* L
 
 unsigned int fwd_read_error(cudaStream_t s) { return read_and_clear_error(s); }
 
+// One thread waits on an mbarrier that is initialised for one arrival and
+// never receives it.  The bounded wait gives up after `limit_ns`, records
+// kSelftestSite in the error word and the kernel returns normally.
+constexpr unsigned int kSelftestSite = 900;
+__global__ void fa_selftest_wait_kernel(unsigned long long limit_ns) {
+  __shared__ __align__(8) uint64_t bar_storage;
+  __shared__ AbortState ab;
+  const uint32_t bar = smem_u32(&bar_storage);
+  mbar_init(bar, 1);
+  ab.flag = 0;
+  fence_barrier_init();
+  mbar_wait_limit(bar, 0, &ab, device_error_word(), kSelftestSite, limit_ns);
+}
+
+fa_status run_selftest_wait(unsigned long long limit_ns, cudaStream_t s) {
+  fa_selftest_wait_kernel<<<1, 1, 0, s>>>(limit_ns);
+  return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
 }  // namespace fa

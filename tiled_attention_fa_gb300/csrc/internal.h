@@ -10,6 +10,7 @@ namespace fa {
 fa_status run_fwd(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int L,
                   int H, int Hkv, int D, int causal, int dtype, cudaStream_t s);
 unsigned int fwd_read_error(cudaStream_t s);
+fa_status run_selftest_wait(unsigned long long limit_ns, cudaStream_t s);
 
 fa_status run_bwd_prep(const void* O, const void* dO, float* Delta, float* dq_accum, int B, int L,
                        int H, int D, int dtype, cudaStream_t s);

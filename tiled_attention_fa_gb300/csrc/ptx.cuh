@@ -87,6 +87,25 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, AbortSt
   }
 }
 
+// Bounded wait with an explicit limit (same protocol as mbar_wait).
+__device__ __forceinline__ bool mbar_wait_limit(uint32_t bar, uint32_t parity, AbortState* ab,
+                                                unsigned int* err_word, unsigned int site,
+                                                unsigned long long limit_ns) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const unsigned long long t0 = globaltimer_ns();
+  for (uint32_t it = 1;; ++it) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((it & 31u) == 0u) {
+      if (*reinterpret_cast<volatile int*>(&ab->flag)) return false;
+      if (globaltimer_ns() - t0 > limit_ns) {
+        *reinterpret_cast<volatile int*>(&ab->flag) = 1;
+        atomicCAS(err_word, 0u, site);
+        return false;
+      }
+    }
+  }
+}
+
 // Bounded wait executed by every lane of a warp; the verdict is made
 // warp-uniform so that later .sync.aligned instructions see the whole warp.
 __device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity, AbortState* ab,
