@@ -34,6 +34,17 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 WORK = dict(B=8, L=4096, H=32, Hkv=32, D=128, dtype="fp16")
+# Named workloads (the default is the headline one); --causal applies on top.
+WORKLOADS = {
+    "b8_h32_l4096_d128": dict(B=8, L=4096, H=32, Hkv=32, D=128, dtype="fp16"),
+    "b1_h2_l128_d64": dict(B=1, L=128, H=2, Hkv=2, D=64, dtype="fp16"),
+    "gqa_b4_h32_hkv8_l4096_d128_bf16": dict(B=4, L=4096, H=32, Hkv=8, D=128, dtype="bf16"),
+    "b8_h32_l1024_d64": dict(B=8, L=1024, H=32, Hkv=32, D=64, dtype="fp16"),
+    "b1_h32_l1024_d128": dict(B=1, L=1024, H=32, Hkv=32, D=128, dtype="fp16"),
+    "b1_h32_l4096_d128": dict(B=1, L=4096, H=32, Hkv=32, D=128, dtype="fp16"),
+    "b1_h32_l8192_d128": dict(B=1, L=8192, H=32, Hkv=32, D=128, dtype="fp16"),
+    "b1_h32_l16384_d128": dict(B=1, L=16384, H=32, Hkv=32, D=128, dtype="fp16"),
+}
 METRIC = "attention fwd/bwd TFLOP/s (fp16 B8 H32 L4096 D128) and % of GB300 TC peak"
 KERNEL_SOURCES = ["tiled_attention_fa_gb300/csrc/ptx.cuh", "tiled_attention_fa_gb300/csrc/common.cuh",
                   "tiled_attention_fa_gb300/csrc/fwd.cuh", "tiled_attention_fa_gb300/csrc/bwd.cuh"]
@@ -222,11 +233,12 @@ def reference_arm(args):
 
 def config_dict(args, world):
     B, L, H, Hkv, D = WORK["B"], WORK["L"], WORK["H"], WORK["Hkv"], WORK["D"]
-    return {"workload": f"attention fwd+bwd B{B} H{H} Hkv{Hkv} L{L} D{D} fp16 "
+    return {"workload": f"attention fwd+bwd B{B} H{H} Hkv{Hkv} L{L} D{D} {WORK['dtype']} "
                         f"{'causal' if args.causal else 'non-causal'}",
             "B": B, "L": L, "H": H, "Hkv": Hkv, "D": D, "causal": bool(args.causal),
             "per_gpu_batch": B, "global_batch": B * world, "parallelism": f"replicas x{world}",
-            "l2": "inputs larger than L2 (Q, K, V, dO 268 MB each)"}
+            "l2": ("inputs larger than L2 (Q, K, V, dO %d MB each)" % (B * L * H * D * 2 // 10**6)
+                   if B * L * H * D * 2 > 129 * 10**6 else "inputs fit in L2 (no flush)")}
 
 
 def ours_arm(args):
@@ -242,7 +254,7 @@ def ours_arm(args):
 
     B, L, H, Hkv, D = WORK["B"], WORK["L"], WORK["H"], WORK["Hkv"], WORK["D"]
     causal = bool(args.causal)
-    dt = torch.float16
+    dt = torch.float16 if WORK["dtype"] == "fp16" else torch.bfloat16
     g = torch.Generator(device=dev).manual_seed(replicas.replica_seed(1234, rank))
     q = torch.randn(B, L, H, D, device=dev, dtype=dt, generator=g)
     k = torch.randn(B, L, Hkv, D, device=dev, dtype=dt, generator=g)
@@ -363,7 +375,7 @@ def ours_arm(args):
         out = {
             "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
-            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "fp16",
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": WORK["dtype"],
             "data": "synthetic", "config": config_dict(args, world),
             "frac_of_peak": {"burst": value / world / burst, "sustained": value / world / sustained,
                              "source": src},
@@ -389,10 +401,13 @@ def main():
     ap.add_argument("--no-clocks", action="store_true",
                     help="skip the nvidia-smi clock sampler (for profiler runs)")
     ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle work")
-    ap.add_argument("--batch", type=int, default=WORK["B"],
-                    help="batch size (smaller values only for profiling captures)")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS), default="b8_h32_l4096_d128")
+    ap.add_argument("--batch", type=int, default=None,
+                    help="override the batch size (smaller values only for profiling captures)")
     args = ap.parse_args()
-    WORK["B"] = args.batch
+    WORK.update(WORKLOADS[args.workload])
+    if args.batch is not None:
+        WORK["B"] = args.batch
     if args.warmup < 3:
         args.warmup = 3
     if args.impl == "reference":
