@@ -26,9 +26,11 @@
 //              Delta_i) through a two-slot ring.
 //   warp  13   TMEM allocator and the single tcgen05.mma issuing thread.
 //   warps 14-15 idle.
-// The score and gradient MMAs are split by query halves, so the tensor core
-// computes half B's S^T/dP^T (and then half A's dV/dK products) while the
-// other warpgroup exponentiates.  dK and dV stay in TMEM for the whole CTA;
+// Per tile the MMA thread issues dP^T for query half A, S^T for all 128
+// queries, then dP^T for half B, so warpgroup A exponentiates while the
+// tensor core computes half B's dP^T (and half A's dV/dK products run while
+// warpgroup B finishes); S^T and dQ are single N=128 MMA groups, keeping the
+// instruction count per tile at 48.  dK and dV stay in TMEM for the whole CTA;
 // for grouped-query attention the CTA loops over every query head of its K/V
 // head, so dK/dV need no atomics.
 #pragma once
@@ -78,16 +80,15 @@ struct BwdLayout {
   static constexpr uint32_t DO_OFF = Q_OFF + STAGES * TILE;   // [STAGES] tiles
   static constexpr uint32_t DS_OFF = DO_OFF + STAGES * TILE;  // 2 chunks (128 keys x 128 queries)
   static constexpr uint32_t SMEM_ALLOC = DS_OFF + 2 * CHUNK;
-  // TMEM columns
-  static constexpr uint32_t TM_DK = 0, TM_DV = D, TM_S = 2 * D, TM_DP = 2 * D + 128;
-  // The dQ tile is produced as D/64 halves of 64 columns.  D=64: its own
-  // columns.  D=128: half 0 sits in the S^T columns of query half B and half
-  // 1 in the dP^T columns of query half B, so the next tile's half-A work
-  // never waits for the dQ drain; each half is released on its own barrier.
+  // TMEM columns: dK | dV | dP^T (queries 0-63) | S^T (128 queries) | dP^T (64-127).
+  // The dQ tile (N = D) is written at column 384: at D=64 that is its own
+  // region; at D=128 it covers S^T's query-half-B columns and the second dP^T
+  // half, so the next tile's first MMA (dP^T of half A) never waits for the dQ
+  // drain; each 64-column dQ half is released on its own barrier.
+  static constexpr uint32_t TM_DK = 0, TM_DV = D, TM_DPA = 2 * D, TM_S = 2 * D + 64,
+                            TM_DPB = 2 * D + 192;
   static constexpr int NDQ = D / 64;
-  __host__ __device__ static constexpr uint32_t tm_dq(int h) {
-    return D == 128 ? (h == 0 ? TM_S + 64 : TM_DP + 64) : (2 * D + 256);
-  }
+  __host__ __device__ static constexpr uint32_t tm_dq(int h) { return 384u + 64u * h; }
   static constexpr uint32_t TMEM_COLS = 512;
   static constexpr int NTHREADS = 512;
 };
@@ -125,9 +126,10 @@ __global__ void __launch_bounds__(512, 1)
                   const BwdParams p) {
   using Ly = BwdLayout<D>;
   using T = typename std::conditional<BF16, __nv_bfloat16, __half>::type;
-  constexpr uint32_t IDESC_SS = idesc_f16(BF16, 128, 64, false, false);  // S^T, dP^T halves
+  constexpr uint32_t IDESC_S = idesc_f16(BF16, 128, 128, false, false);  // S^T, all queries
+  constexpr uint32_t IDESC_DP = idesc_f16(BF16, 128, 64, false, false);  // dP^T, one query half
   constexpr uint32_t IDESC_KN = idesc_f16(BF16, 128, D, false, true);    // dV (A tmem), dK
-  constexpr uint32_t IDESC_MN = idesc_f16(BF16, 128, 64, true, true);    // dQ halves
+  constexpr uint32_t IDESC_MN = idesc_f16(BF16, 128, D, true, true);     // dQ
 
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   const uint32_t base = smem_u32(smem_raw);
@@ -241,34 +243,35 @@ __global__ void __launch_bounds__(512, 1)
         tc_fence_after();
         const uint32_t qa = base + Ly::Q_OFF + stage * Ly::TILE;
         const uint32_t doa = base + Ly::DO_OFF + stage * Ly::TILE;
-        // Scores and score gradients, one 64-query half at a time:
-        //   S^T_c = K_j Q_c^T, dP^T_c = V_j dO_c^T  (keys x 64 queries)
-#pragma unroll
-        for (int c = 0; c < 2; ++c) {
-          const uint32_t roff = c * 8192u;  // query rows 64c.. start 64 rows into each chunk
-          // D=128: half B's S^T / dP^T columns held the previous tile's dQ halves.
-          if (D == 128 && c == 1 && n > 0) {
-            if (!mbar_wait(bar(Ly::B_DQEMPTY), (n - 1) & 1, ab, err, 503)) { ok = false; break; }
-            tc_fence_after();
-          }
+        // dP^T_A = V_j dO_A^T (queries 0-63), S^T = K_j Q_i^T (all queries),
+        // dP^T_B = V_j dO_B^T (queries 64-127).  Half A's softmax starts after
+        // the first two, overlapping dP^T_B and half B's work.
+        auto issue_dp = [&](int c, uint32_t dst) {
 #pragma unroll
           for (int k = 0; k < D / 16; ++k) {
             const uint32_t off = (k >> 2) * Ly::CHUNK + (k & 3) * 32u;
-            mma_ss(tmem + Ly::TM_S + 64 * c, sdesc_sw128(ka + off, 16, 1024),
-                   sdesc_sw128(qa + off + roff, 16, 1024), IDESC_SS, k > 0 ? 1u : 0u);
+            mma_ss(dst, sdesc_sw128(va + off, 16, 1024),
+                   sdesc_sw128(doa + off + c * 8192u, 16, 1024), IDESC_DP, k > 0 ? 1u : 0u);
           }
-          if (D == 128 && c == 1 && n > 0) {
-            if (!mbar_wait(bar(Ly::B_DQEMPTY + 1), (n - 1) & 1, ab, err, 507)) { ok = false; break; }
-            tc_fence_after();
-          }
-#pragma unroll
-          for (int k = 0; k < D / 16; ++k) {
-            const uint32_t off = (k >> 2) * Ly::CHUNK + (k & 3) * 32u;
-            mma_ss(tmem + Ly::TM_DP + 64 * c, sdesc_sw128(va + off, 16, 1024),
-                   sdesc_sw128(doa + off + roff, 16, 1024), IDESC_SS, k > 0 ? 1u : 0u);
-          }
-          tc_commit(bar(Ly::B_SFULL + c));
+        };
+        issue_dp(0, tmem + Ly::TM_DPA);
+        if (D == 128 && n > 0) {  // dQ half 0 of the previous tile sits in S^T's upper half
+          if (!mbar_wait(bar(Ly::B_DQEMPTY), (n - 1) & 1, ab, err, 503)) { ok = false; break; }
+          tc_fence_after();
         }
+#pragma unroll
+        for (int k = 0; k < D / 16; ++k) {
+          const uint32_t off = (k >> 2) * Ly::CHUNK + (k & 3) * 32u;
+          mma_ss(tmem + Ly::TM_S, sdesc_sw128(ka + off, 16, 1024), sdesc_sw128(qa + off, 16, 1024),
+                 IDESC_S, k > 0 ? 1u : 0u);
+        }
+        tc_commit(bar(Ly::B_SFULL));
+        if (D == 128 && n > 0) {  // dQ half 1 sits in dP^T_B's columns
+          if (!mbar_wait(bar(Ly::B_DQEMPTY + 1), (n - 1) & 1, ab, err, 507)) { ok = false; break; }
+          tc_fence_after();
+        }
+        issue_dp(1, tmem + Ly::TM_DPB);
+        tc_commit(bar(Ly::B_SFULL + 1));
         if (!ok) break;
         // dV += P^T_c dO_c and dK += dS^T_c Q_c as each half's P^T / dS^T lands.
 #pragma unroll
@@ -291,15 +294,11 @@ __global__ void __launch_bounds__(512, 1)
           if (!mbar_wait(bar(Ly::B_DQEMPTY), (n - 1) & 1, ab, err, 506)) { ok = false; break; }
           tc_fence_after();
         }
-        // dQ_i = dS K_j in 64-column halves (dS read MN-major from the dS^T
-        // tile, K_j MN-major).
+        // dQ_i = dS K_j   (dS read MN-major from the dS^T tile, K_j MN-major)
 #pragma unroll
-        for (int hq = 0; hq < Ly::NDQ; ++hq)
-#pragma unroll
-          for (int k = 0; k < 8; ++k)
-            mma_ss(tmem + Ly::tm_dq(hq), sdesc_sw128(dsa + 2048u * k, Ly::CHUNK, 1024),
-                   sdesc_sw128(ka + hq * Ly::CHUNK + 2048u * k, Ly::CHUNK, 1024), IDESC_MN,
-                   k > 0 ? 1u : 0u);
+        for (int k = 0; k < 8; ++k)
+          mma_ss(tmem + Ly::tm_dq(0), sdesc_sw128(dsa + 2048u * k, Ly::CHUNK, 1024),
+                 sdesc_sw128(ka + 2048u * k, Ly::CHUNK, 1024), IDESC_MN, k > 0 ? 1u : 0u);
         tc_commit(bar(Ly::B_DQFULL));
         tc_commit(bar(Ly::B_QEMPTY + stage));
         if (++stage == Ly::STAGES) {
@@ -318,7 +317,7 @@ __global__ void __launch_bounds__(512, 1)
     const int kr = it.j * 128 + r;
     const uint32_t lane_off = ((warp & 3u) * 32u) << 16;
     const uint32_t tS = tmem + lane_off + Ly::TM_S + 64 * hc;
-    const uint32_t tP = tmem + lane_off + Ly::TM_DP + 64 * hc;
+    const uint32_t tP = tmem + lane_off + (hc ? Ly::TM_DPB : Ly::TM_DPA);
     const float sl2 = p.sl2;
     uint8_t* ds_row = smem_raw + Ly::DS_OFF + hc * Ly::CHUNK + r * 128;
     bool ok = true;
