@@ -12,13 +12,15 @@
 //
 // GB300 design of the main pass (512 threads, one CTA per SM, one K/V tile
 // of 128 keys per CTA):
-//   warps 0-3  compute warpgroup A: query columns 0-63 of every Q tile;
-//   warps 4-7  compute warpgroup B: query columns 64-127.  In both, thread r
-//              owns key row r (its TMEM lane) and forms
+//   warps 0-7  compute warps: each query half of a tile (columns 0-63, then
+//              64-127) is split over all eight, warp w taking 32 columns
+//              of key rows 32*(w%4).. (its TMEM lanes); a thread owns one
+//              key row and forms
 //              P^T = exp2(S^T*c - LSE*log2e) and dS^T = P^T o (dP^T - Delta);
 //              P^T goes back to TMEM (A operand of dV += P^T dO), dS^T to a
 //              swizzled smem tile (A operand of dK += dS^T Q and, read
-//              MN-major, of dQ = dS K).  At the end A writes dK and B dV.
+//              MN-major, of dQ = dS K).  At the end warps 0-3 write dK and
+//              warps 4-7 dV.
 //   warps 8-11 dQ drain: thread r owns query row r; reads the dQ tile from
 //              TMEM and adds it into the fp32 accumulator with 16-byte
 //              vector atomics.
@@ -154,7 +156,7 @@ __global__ void __launch_bounds__(512, 1)
     }
     for (int c = 0; c < 2; ++c) {
       mbar_init(bar(Ly::B_SFULL + c), 1);
-      mbar_init(bar(Ly::B_PFULL + c), 128);
+      mbar_init(bar(Ly::B_PFULL + c), 256);
     }
     mbar_init(bar(Ly::B_DQFULL), 1);
     mbar_init(bar(Ly::B_DQEMPTY), 128);
@@ -280,7 +282,7 @@ __global__ void __launch_bounds__(512, 1)
           tc_fence_after();
 #pragma unroll
           for (int k = 0; k < 4; ++k)
-            mma_ts(tmem + Ly::TM_DV, tmem + Ly::TM_S + 64 * c + 8u * k,
+            mma_ts(tmem + Ly::TM_DV, tmem + Ly::TM_S + 64 * c + (k >> 1) * 32u + (k & 1) * 8u,
                    sdesc_sw128(doa + 2048u * (4 * c + k), Ly::CHUNK, 1024), IDESC_KN,
                    (n > 0 || c > 0 || k > 0) ? 1u : 0u);
 #pragma unroll
@@ -311,39 +313,42 @@ __global__ void __launch_bounds__(512, 1)
       mbar_wait_drain(bar(Ly::B_DONE), 0);
     }
   } else if (warp < 8) {
-    // ------------------------------------------------------------ P^T / dS^T (one query half)
-    const int hc = warp >> 2;         // query half of this warpgroup
+    // ------------------------------------------------------------ P^T / dS^T
+    // All eight warps work on query half A, then on half B: warp w owns key
+    // rows 32*(w%4).. (its TMEM lanes) and the 32-query chunk sub = w/4 of the
+    // current half.
+    const int sub = warp >> 2;        // 32-query chunk within a half
     const int r = threadIdx.x & 127;  // key row within the tile == TMEM lane
     const int kr = it.j * 128 + r;
     const uint32_t lane_off = ((warp & 3u) * 32u) << 16;
-    const uint32_t tS = tmem + lane_off + Ly::TM_S + 64 * hc;
-    const uint32_t tP = tmem + lane_off + (hc ? Ly::TM_DPB : Ly::TM_DPA);
     const float sl2 = p.sl2;
-    uint8_t* ds_row = smem_raw + Ly::DS_OFF + hc * Ly::CHUNK + r * 128;
     bool ok = true;
     uint32_t stage = 0;
-    for (int n = 0; n < ntiles; ++n) {
+    for (int n = 0; ok && n < ntiles; ++n) {
       int h, i;
       bwd_tile(it, p, n, h, i);
-      if (!mbar_wait_warp(bar(Ly::B_SFULL + hc), n & 1, ab, err, 601)) { ok = false; break; }
-      tc_fence_after();
-      const float* st = stats + stage * 256 + 64 * hc;
-      const int q0 = i * 128 + 64 * hc;
-      // query columns [lo, hi) of this half are visible to key kr
-      int lo = 0, hi = min(64, p.L - q0);
-      if (kr >= p.L) hi = 0;
-      if (p.causal) lo = max(0, kr - q0);
-      const bool full = (lo == 0 && hi == 64);
 #pragma unroll
-      for (int ch = 0; ch < 2; ++ch) {  // 32 query columns per chunk
-        uint32_t s[32], dp[32];
-        tmem_ld32(tS + 32 * ch, s);
-        tmem_ld32(tP + 32 * ch, dp);
-        tmem_ld_wait32(s);
+      for (int hc = 0; hc < 2; ++hc) {
+        if (!mbar_wait_warp(bar(Ly::B_SFULL + hc), n & 1, ab, err, 601)) { ok = false; break; }
+        tc_fence_after();
+        const int cbase = 64 * hc + 32 * sub;  // first query column of this chunk
+        const uint32_t tS = tmem + lane_off + Ly::TM_S + cbase;
+        const uint32_t tP = tmem + lane_off + (hc ? Ly::TM_DPB : Ly::TM_DPA) + 32 * sub;
+        const float* st = stats + stage * 256 + cbase;
+        const int q0 = i * 128 + cbase;
+        // query columns [lo, hi) of this chunk are visible to key kr
+        int lo = 0, hi = min(32, p.L - q0);
+        if (kr >= p.L) hi = 0;
+        if (p.causal) lo = max(0, kr - q0);
+        const bool full = (lo == 0 && hi == 32);
+        uint32_t sv[32], dp[32];
+        tmem_ld32(tS, sv);
+        tmem_ld32(tP, dp);
+        tmem_ld_wait32(sv);
         tmem_ld_wait32(dp);
         uint32_t pk[16], dk[16];
-        const float4* st4 = reinterpret_cast<const float4*>(st + 32 * ch);
-        const float4* dl4 = reinterpret_cast<const float4*>(st + 128 + 32 * ch);
+        const float4* st4 = reinterpret_cast<const float4*>(st);
+        const float4* dl4 = reinterpret_cast<const float4*>(st + 128);
 #pragma unroll
         for (int u4 = 0; u4 < 8; ++u4) {
           const float4 l4 = st4[u4], d4 = dl4[u4];
@@ -353,11 +358,8 @@ __global__ void __launch_bounds__(512, 1)
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
             const int cl = 4 * u4 + e;
-            float pp = ex2(fmaf(__uint_as_float(s[cl]), sl2, -lse[e]));
-            if (!full) {
-              const int c = 32 * ch + cl;
-              pp = (c >= lo && c < hi) ? pp : 0.f;
-            }
+            float pp = ex2(fmaf(__uint_as_float(sv[cl]), sl2, -lse[e]));
+            if (!full) pp = (cl >= lo && cl < hi) ? pp : 0.f;
             pv[e] = pp;
             dv[e] = pp * (__uint_as_float(dp[cl]) - dlt[e]);
           }
@@ -366,22 +368,24 @@ __global__ void __launch_bounds__(512, 1)
           dk[2 * u4] = pack2<T>(dv[0], dv[1]);
           dk[2 * u4 + 1] = pack2<T>(dv[2], dv[3]);
         }
-        // P^T columns (16-bit pairs) overwrite S^T columns already read.
-        tmem_st16(tS + 16 * ch, pk);
-        // dS^T row r, queries 64*hc + 32*ch .. +31: four swizzled 16-byte units.
+        // P^T (16-bit pairs) over the first 16 of this chunk's own S^T columns.
+        tmem_st16(tS, pk);
+        // dS^T row r, queries cbase .. cbase+31: four swizzled 16-byte units.
+        uint8_t* ds_row = smem_raw + Ly::DS_OFF + hc * Ly::CHUNK + r * 128;
 #pragma unroll
         for (int v = 0; v < 4; ++v) {
-          const int pos = (ch * 4 + v) ^ (r & 7);
+          const int pos = (sub * 4 + v) ^ (r & 7);
           *reinterpret_cast<uint4*>(ds_row + pos * 16) =
               make_uint4(dk[4 * v], dk[4 * v + 1], dk[4 * v + 2], dk[4 * v + 3]);
         }
+        tmem_st_wait();
+        fence_proxy_async_smem();
+        tc_fence_before();
+        mbar_arrive(bar(Ly::B_PFULL + hc));
       }
-      tmem_st_wait();
-      fence_proxy_async_smem();
-      tc_fence_before();
-      mbar_arrive(bar(Ly::B_PFULL + hc));
       if (++stage == Ly::STAGES) stage = 0;
     }
+    const int hc = sub;  // epilogue role: warps 0-3 write dK, warps 4-7 write dV
     // Epilogue: warpgroup A writes dK (scaled by 1/sqrt(D)), B writes dV.
     if (ok && mbar_wait_warp(bar(Ly::B_DKVFULL), 0, ab, err, 602)) {
       tc_fence_after();
