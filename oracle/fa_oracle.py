@@ -14,10 +14,16 @@ softmax, no fusion):
   reference function described on the same page:
 
       S = Q_bh K_{b,hk}^T / sqrt(D)              (full L x L matrix)
-      S[i, j] = -inf  for j > i                   (causal, top-left aligned)
+      S[i, j] = -inf  for j > i + past_len        (causal; past_len = Lk - Lq)
       m_i = max_j S_ij
       P_ij = exp(S_ij - m_i) / sum_j exp(S_ij - m_i)   (two-pass softmax)
       O = P V_{b,hk}                              (explicit matmul)
+
+  Queries may be fewer than keys (Lq <= Lk): following the causal-mask
+  section of "TileLang性能分析报告：H100上FlashAttention吞吐量达1.2PFlops"
+  (query index = row + past_len, key visible iff query index >= key index)
+  with past_len = Lk - Lq, i.e. the queries are the last Lq positions of the
+  Lk-long sequence (bottom-right aligned; top-left when Lq = Lk).
 
   with the grouped-query head map hk = h // (H // Hkv): the page's kernel
   reads the K/V head whose index is the query head divided by the group
@@ -104,19 +110,19 @@ def _as64(x) -> np.ndarray:
 
 
 def unit_scores(q_bh: np.ndarray, k_bh: np.ndarray, causal: bool,
-                row0: int = 0) -> np.ndarray:
+                row0: int = 0, past: int = 0) -> np.ndarray:
     """Scaled, masked score rows S[row0:row0+n, :] for one (b, h).
 
-    q_bh: [n, D] query rows row0..row0+n-1; k_bh: [L, D] all keys.
-    Causal masking is top-left aligned: key j is visible to query i iff j <= i.
+    q_bh: [n, D] query rows row0..row0+n-1; k_bh: [Lk, D] all keys.
+    Causal: key j is visible to query i iff j <= i + past.
     """
     n, D = q_bh.shape
-    L = k_bh.shape[0]
+    Lk = k_bh.shape[0]
     S = (q_bh @ k_bh.T) / np.sqrt(D)
     if causal:
         i = np.arange(row0, row0 + n)[:, None]
-        j = np.arange(L)[None, :]
-        S = np.where(j > i, -np.inf, S)
+        j = np.arange(Lk)[None, :]
+        S = np.where(j > i + past, -np.inf, S)
     return S
 
 
@@ -131,19 +137,21 @@ def _softmax_rows(S: np.ndarray):
 def unit_forward(q_bh, k_bh, v_bh, causal: bool, rows=None, panel: int = 4096):
     """O and LSE rows of one (b, h).
 
-    q_bh [L, D], k_bh / v_bh [L, D] (already the K/V head this query head
-    reads).  ``rows`` (optional int array) restricts the output to those query
-    rows; the keys are always all L.  Returns (O [n, D], LSE [n]).
+    q_bh [Lq, D], k_bh / v_bh [Lk, D] (already the K/V head this query head
+    reads), Lq <= Lk under causal masking.  ``rows`` (optional int array)
+    restricts the output to those query rows; the keys are always all Lk.
+    Returns (O [n, D], LSE [n]).
     """
     q_bh, k_bh, v_bh = _as64(q_bh), _as64(k_bh), _as64(v_bh)
-    L = q_bh.shape[0]
-    rows = np.arange(L) if rows is None else np.asarray(rows)
+    Lq, Lk = q_bh.shape[0], k_bh.shape[0]
+    past = Lk - Lq
+    rows = np.arange(Lq) if rows is None else np.asarray(rows)
     outs_o, outs_l = [], []
     for p0 in range(0, len(rows), panel):
         r = rows[p0:p0 + panel]
         S = (q_bh[r] @ k_bh.T) / np.sqrt(q_bh.shape[1])
         if causal:
-            S = np.where(np.arange(L)[None, :] > r[:, None], -np.inf, S)
+            S = np.where(np.arange(Lk)[None, :] > r[:, None] + past, -np.inf, S)
         P, m, s = _softmax_rows(S)
         outs_o.append(P @ v_bh)
         outs_l.append(m + np.log(s))
@@ -155,25 +163,28 @@ def unit_forward(q_bh, k_bh, v_bh, causal: bool, rows=None, panel: int = 4096):
 def unit_backward(q_bh, k_bh, v_bh, do_bh, causal: bool, panel: int = 4096, o_round=None):
     """Gradients of one (b, h) pair against its K/V head.
 
-    Returns (dQ [L, D], dK [L, D], dV [L, D], Delta [L], O [L, D], LSE [L]).
+    q_bh, do_bh [Lq, D]; k_bh, v_bh [Lk, D] (Lq <= Lk under causal masking).
+    Returns (dQ [Lq, D], dK [Lk, D], dV [Lk, D], Delta [Lq], O [Lq, D], LSE [Lq]).
     The oracle recomputes its own O and Delta; nothing comes from a kernel.
     ``o_round`` (None, "fp16", "bf16") is the storage format of the O that
     Delta is formed from.
     """
     q_bh, k_bh, v_bh, do_bh = (_as64(x) for x in (q_bh, k_bh, v_bh, do_bh))
-    L, D = q_bh.shape
+    Lq, D = q_bh.shape
+    Lk = k_bh.shape[0]
+    past = Lk - Lq
     inv = 1.0 / np.sqrt(D)
-    dq = np.zeros((L, D))
-    dk = np.zeros((L, D))
-    dv = np.zeros((L, D))
-    o = np.zeros((L, D))
-    lse = np.zeros((L,))
-    delta = np.zeros((L,))
-    for r0 in range(0, L, panel):
-        r = np.arange(r0, min(L, r0 + panel))
+    dq = np.zeros((Lq, D))
+    dk = np.zeros((Lk, D))
+    dv = np.zeros((Lk, D))
+    o = np.zeros((Lq, D))
+    lse = np.zeros((Lq,))
+    delta = np.zeros((Lq,))
+    for r0 in range(0, Lq, panel):
+        r = np.arange(r0, min(Lq, r0 + panel))
         S = (q_bh[r] @ k_bh.T) * inv
         if causal:
-            S = np.where(np.arange(L)[None, :] > r[:, None], -np.inf, S)
+            S = np.where(np.arange(Lk)[None, :] > r[:, None] + past, -np.inf, S)
         P, m, s = _softmax_rows(S)
         O = P @ v_bh
         o[r] = O
@@ -192,8 +203,8 @@ def unit_backward(q_bh, k_bh, v_bh, do_bh, causal: bool, panel: int = 4096, o_ro
 def forward(q, k, v, causal: bool):
     """Full forward over BSHD tensors.
 
-    q [B, L, H, D]; k, v [B, L, Hkv, D].  Returns O [B, L, H, D] and
-    LSE [B, H, L] (float64).
+    q [B, Lq, H, D]; k, v [B, Lk, Hkv, D].  Returns O [B, Lq, H, D] and
+    LSE [B, H, Lq] (float64).
     """
     q, k, v = _as64(q), _as64(k), _as64(v)
     B, L, H, D = q.shape
@@ -217,15 +228,16 @@ def bwd_preprocess(o, do):
 def backward(q, k, v, do, causal: bool, o_round=None):
     """Full backward over BSHD tensors.
 
-    Returns dQ [B, L, H, D], dK [B, L, Hkv, D], dV [B, L, Hkv, D],
-    Delta [B, H, L] (from the oracle's own O, rounded to ``o_round`` if given).
+    q, do [B, Lq, H, D]; k, v [B, Lk, Hkv, D].  Returns dQ [B, Lq, H, D],
+    dK [B, Lk, Hkv, D], dV [B, Lk, Hkv, D], Delta [B, H, Lq] (from the
+    oracle's own O, rounded to ``o_round`` if given).
     """
     q, k, v, do = _as64(q), _as64(k), _as64(v), _as64(do)
     B, L, H, D = q.shape
-    Hkv = k.shape[2]
+    Lk, Hkv = k.shape[1], k.shape[2]
     dq = np.zeros((B, L, H, D))
-    dk = np.zeros((B, L, Hkv, D))
-    dv = np.zeros((B, L, Hkv, D))
+    dk = np.zeros((B, Lk, Hkv, D))
+    dv = np.zeros((B, Lk, Hkv, D))
     delta = np.zeros((B, H, L))
     for b in range(B):
         for h in range(H):

@@ -438,3 +438,91 @@ def test_rounded_delta_only_moves_delta():
     bound = 2.0 ** -9 * np.einsum("blhd->bhl", np.abs(o * do))
     assert np.all(np.abs(d1 - d0) <= bound + 1e-15)
     assert np.abs(d1 - d0).max() > 0
+
+
+# ---------------------------------------------------------------- fewer queries than keys
+
+def _suffix_case(seed, B=1, L=23, Lq=7, H=2, Hkv=1, D=8):
+    rng = np.random.default_rng(seed)
+    q = rng.standard_normal((B, L, H, D))
+    k = rng.standard_normal((B, L, Hkv, D))
+    v = rng.standard_normal((B, L, Hkv, D))
+    do = rng.standard_normal((B, L, H, D))
+    do[:, : L - Lq] = 0.0       # only the last Lq query rows carry a gradient
+    return q, k, v, do, Lq
+
+
+def test_suffix_queries_match_the_full_causal_problem():
+    # The last Lq rows of a causal L x L problem are the (Lq, Lk=L) problem with
+    # past_len = L - Lq: same O, LSE; with dO zero on the other rows, same dQ
+    # rows and the same dK, dV.
+    q, k, v, do, Lq = _suffix_case(90)
+    L = q.shape[1]
+    o_full, l_full = orc.forward(q, k, v, True)
+    o_suf, l_suf = orc.forward(q[:, L - Lq:], k, v, True)
+    np.testing.assert_allclose(o_suf, o_full[:, L - Lq:], atol=1e-13)
+    np.testing.assert_allclose(l_suf, l_full[:, :, L - Lq:], atol=1e-13)
+    dq_f, dk_f, dv_f, _ = orc.backward(q, k, v, do, True)
+    dq_s, dk_s, dv_s, _ = orc.backward(q[:, L - Lq:], k, v, do[:, L - Lq:], True)
+    np.testing.assert_allclose(dq_s, dq_f[:, L - Lq:], atol=1e-13)
+    np.testing.assert_allclose(dk_s, dk_f, atol=1e-13)
+    np.testing.assert_allclose(dv_s, dv_f, atol=1e-13)
+
+
+def test_single_query_causal_sees_every_key():
+    rng = np.random.default_rng(91)
+    q, k, v = rng.standard_normal((1, 8)), rng.standard_normal((30, 8)), rng.standard_normal((30, 8))
+    oc, lc = orc.unit_forward(q, k, v, True)
+    on, ln_ = orc.unit_forward(q, k, v, False)
+    np.testing.assert_allclose(oc, on, atol=1e-14)
+    np.testing.assert_allclose(lc, ln_, atol=1e-14)
+
+
+def test_fewer_queries_non_causal_matches_torch():
+    rng = np.random.default_rng(92)
+    B, Lq, Lk, H, Hkv, D = 2, 9, 21, 4, 2, 16
+    q, k, v, do = (rng.standard_normal(s) for s in ((B, Lq, H, D), (B, Lk, Hkv, D), (B, Lk, Hkv, D), (B, Lq, H, D)))
+    o, _ = orc.forward(q, k, v, False)
+    dq, dk, dv, _ = orc.backward(q, k, v, do, False)
+    to, tdq, tdk, tdv = torch_reference(q, k, v, do, False)
+    for a, b in ((o, to), (dq, tdq), (dk, tdk), (dv, tdv)):
+        np.testing.assert_allclose(a, b, atol=1e-11, rtol=1e-9)
+
+
+def test_fewer_queries_gradients_match_finite_differences():
+    rng = np.random.default_rng(93)
+    B, Lq, Lk, H, Hkv, D = 1, 3, 6, 2, 1, 4
+    q, k, v, do = (rng.standard_normal(s) for s in ((B, Lq, H, D), (B, Lk, Hkv, D), (B, Lk, Hkv, D), (B, Lq, H, D)))
+    dq, dk, dv, _ = orc.backward(q, k, v, do, True)
+
+    def f(qq, kk, vv):
+        return float((orc.forward(qq, kk, vv, True)[0] * do).sum())
+    eps = 1e-6
+    for i, (x, g) in enumerate(((q, dq), (k, dk), (v, dv))):
+        num = np.zeros_like(x)
+        for idx in np.ndindex(x.shape):
+            args_p, args_m = [q, k, v], [q, k, v]
+            xp, xm = x.copy(), x.copy()
+            xp[idx] += eps
+            xm[idx] -= eps
+            args_p[i], args_m[i] = xp, xm
+            num[idx] = (f(*args_p) - f(*args_m)) / (2 * eps)
+        assert np.abs(num - g).max() / max(1.0, np.abs(g).max()) < 1e-6
+
+
+def test_top_left_alignment_is_caught():
+    # A planted mistake: aligning the causal mask top-left for Lq < Lk.
+    q, k, v, _, Lq = _suffix_case(94)
+    L = q.shape[1]
+
+    def top_left(q_bh, k_bh, v_bh):
+        S = unit_scores_top_left(q_bh, k_bh)
+        P = np.exp(S - S.max(axis=1, keepdims=True))
+        return (P / P.sum(axis=1, keepdims=True)) @ v_bh
+
+    def unit_scores_top_left(q_bh, k_bh):
+        return orc.unit_scores(q_bh, k_bh, True, past=0)
+
+    o_full, _ = orc.forward(q, k, v, True)
+    wrong = top_left(q[0, L - Lq:, 0], k[0, :, 0], v[0, :, 0])
+    assert not np.allclose(wrong, o_full[0, L - Lq:, 0], atol=1e-6)
