@@ -56,6 +56,19 @@ fa_status fa_fwd(const void* Q, const void* K, const void* V, void* O, float* LS
                  int H, int Hkv, int D, int causal, int dtype, void* stream);
 
 /*
+ * Forward with fewer queries than keys (prefill against a key/value cache):
+ * Q, O [B, Lq, H, D]; K, V [B, Lk, Hkv, D]; LSE [B, H, Lq].  Under causal
+ * masking the queries are the last Lq positions of the Lk-long sequence:
+ * query i sees key j iff j <= i + past_len with past_len = Lk - Lq (page
+ * "TileLang性能分析报告：H100上FlashAttention吞吐量达1.2PFlops", section
+ * 因果掩码优化, where the query index is the row plus past_len); causal
+ * calls need Lk >= Lq.  Non-causal calls accept any Lq, Lk >= 1.  With
+ * Lq == Lk this is fa_fwd.
+ */
+fa_status fa_fwd_kv(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int Lq,
+                    int Lk, int H, int Hkv, int D, int causal, int dtype, void* stream);
+
+/*
  * Backward preprocess: Delta[b, h, i] = sum_d O[b, i, h, d] * dO[b, i, h, d]
  * (fp32 accumulation), the per-row term of the softmax gradient.  Page
  * "TileLang与机器学习训练：反向传播算子优化案例", section 算子拆分与流水线设计
@@ -91,6 +104,17 @@ fa_status fa_bwd(const void* Q, const void* K, const void* V, const void* O, con
                  const float* LSE, const float* Delta, void* dQ, void* dK, void* dV,
                  float* dq_accum, int zero_accum, int B, int L, int H, int Hkv, int D, int causal,
                  int dtype, void* stream);
+
+/*
+ * Backward of fa_fwd_kv: Q, O, dO, dQ [B, Lq, H, D]; K, V, dK, dV
+ * [B, Lk, Hkv, D]; LSE, Delta [B, H, Lq]; dq_accum of
+ * fa_bwd_workspace_size(B, Lq, H, D) bytes (fa_bwd_preprocess with L = Lq
+ * computes Delta and zeroes it).  Same masking rule and limits as fa_fwd_kv.
+ */
+fa_status fa_bwd_kv(const void* Q, const void* K, const void* V, const void* O, const void* dO,
+                    const float* LSE, const float* Delta, void* dQ, void* dK, void* dV,
+                    float* dq_accum, int zero_accum, int B, int Lq, int Lk, int H, int Hkv, int D,
+                    int causal, int dtype, void* stream);
 
 /*
  * The two stages fa_bwd runs, for callers that schedule or time them apart:

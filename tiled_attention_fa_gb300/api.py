@@ -41,12 +41,15 @@ def _stream(stream) -> int:
 
 
 def fwd(q, k, v, causal: bool = False, out=None, lse=None, stream=None):
-    """O, LSE = attention(Q, K, V).  q [B, L, H, D]; k, v [B, L, Hkv, D]."""
+    """O, LSE = attention(Q, K, V).  q [B, Lq, H, D]; k, v [B, Lk, Hkv, D].
+
+    Lq < Lk means the queries are the last Lq positions (causal offset
+    Lk - Lq); Lq == Lk is the square case."""
     B, L, H, D = q.shape
-    Hkv = k.shape[2]
+    Lk, Hkv = k.shape[1], k.shape[2]
     _need(q, "q")
-    _need(k, "k", (B, L, Hkv, D), q.dtype)
-    _need(v, "v", (B, L, Hkv, D), q.dtype)
+    _need(k, "k", (B, Lk, Hkv, D), q.dtype)
+    _need(v, "v", (B, Lk, Hkv, D), q.dtype)
     if out is None:
         out = torch.empty_like(q)
     if lse is None:
@@ -54,9 +57,15 @@ def fwd(q, k, v, causal: bool = False, out=None, lse=None, stream=None):
     _need(out, "out", q.shape, q.dtype)
     _need(lse, "lse", (B, H, L), torch.float32)
     lib = _lib.load()
-    st = lib.fa_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
-                    B, L, H, Hkv, D, int(bool(causal)), _dtype_code(q), _stream(stream))
-    _lib.check("fa_fwd", st)
+    if Lk == L:
+        st = lib.fa_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
+                        B, L, H, Hkv, D, int(bool(causal)), _dtype_code(q), _stream(stream))
+        _lib.check("fa_fwd", st)
+    else:
+        st = lib.fa_fwd_kv(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                           lse.data_ptr(), B, L, Lk, H, Hkv, D, int(bool(causal)),
+                           _dtype_code(q), _stream(stream))
+        _lib.check("fa_fwd_kv", st)
     return out, lse
 
 
@@ -95,9 +104,9 @@ def bwd(q, k, v, o, do, lse, delta, causal: bool = False, dq=None, dk=None, dv=N
     """dQ, dK, dV of the forward.  ``dq_accum`` is the fp32 workspace; unless
     ``accum_zeroed`` (fa_bwd_preprocess zeroed it) the call zeroes it first."""
     B, L, H, D = q.shape
-    Hkv = k.shape[2]
+    Lk, Hkv = k.shape[1], k.shape[2]
     _need(q, "q")
-    for name, t, shp in (("k", k, (B, L, Hkv, D)), ("v", v, (B, L, Hkv, D)), ("do", do, q.shape)):
+    for name, t, shp in (("k", k, (B, Lk, Hkv, D)), ("v", v, (B, Lk, Hkv, D)), ("do", do, q.shape)):
         _need(t, name, shp, q.dtype)
     _need(lse, "lse", (B, H, L), torch.float32)
     _need(delta, "delta", (B, H, L), torch.float32)
@@ -113,12 +122,17 @@ def bwd(q, k, v, o, do, lse, delta, causal: bool = False, dq=None, dk=None, dv=N
     _need(dq_accum, "dq_accum", dtype=torch.float32)
     if dq_accum.numel() * 4 < workspace_size(B, L, H, D):
         raise ValueError("dq_accum is smaller than workspace_size()")
-    st = _lib.load().fa_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(),
-                            o.data_ptr() if o is not None else None, do.data_ptr(),
-                            lse.data_ptr(), delta.data_ptr(), dq.data_ptr(), dk.data_ptr(),
-                            dv.data_ptr(), dq_accum.data_ptr(), 0 if accum_zeroed else 1,
-                            B, L, H, Hkv, D, int(bool(causal)), _dtype_code(q), _stream(stream))
-    _lib.check("fa_bwd", st)
+    lib = _lib.load()
+    ptrs = (q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr() if o is not None else None,
+            do.data_ptr(), lse.data_ptr(), delta.data_ptr(), dq.data_ptr(), dk.data_ptr(),
+            dv.data_ptr(), dq_accum.data_ptr(), 0 if accum_zeroed else 1)
+    if Lk == L:
+        st = lib.fa_bwd(*ptrs, B, L, H, Hkv, D, int(bool(causal)), _dtype_code(q), _stream(stream))
+        _lib.check("fa_bwd", st)
+    else:
+        st = lib.fa_bwd_kv(*ptrs, B, L, Lk, H, Hkv, D, int(bool(causal)), _dtype_code(q),
+                           _stream(stream))
+        _lib.check("fa_bwd_kv", st)
     return dq, dk, dv
 
 

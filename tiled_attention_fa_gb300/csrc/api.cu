@@ -12,18 +12,24 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 
 bool ptr_ok(const void* p) { return p != nullptr && aligned16(p); }
 
-fa_status check_shape(int B, int L, int H, int Hkv, int D, int dtype) {
-  if (B < 1 || L < 1 || H < 1 || Hkv < 1) return FA_ERR_INVALID_ARG;
-  if (L > (1 << 30) || H > (1 << 20) || B > (1 << 20)) return FA_ERR_INVALID_ARG;
+// Lq query rows, Lk key rows (equal for the square entry points).
+fa_status check_shape(int B, int Lq, int Lk, int H, int Hkv, int D, int dtype) {
+  if (B < 1 || Lq < 1 || Lk < 1 || H < 1 || Hkv < 1) return FA_ERR_INVALID_ARG;
+  if (Lq > (1 << 30) || Lk > (1 << 30) || H > (1 << 20) || B > (1 << 20)) return FA_ERR_INVALID_ARG;
   if (H % Hkv != 0) return FA_ERR_INVALID_ARG;
   if (dtype != FA_F16 && dtype != FA_BF16) return FA_ERR_UNSUPPORTED;
   if (D != 64 && D != 128) return FA_ERR_UNSUPPORTED;
   // Work-item and element counts must fit the kernels' integer arithmetic.
-  const long long items = static_cast<long long>(B) * H * ((L + 255) / 256);
-  const long long elems = static_cast<long long>(B) * fa::padded_len(L) * H * D;
+  const int Lmax = Lq > Lk ? Lq : Lk;
+  const long long items = static_cast<long long>(B) * H * ((Lmax + 127) / 128);
+  const long long elems = static_cast<long long>(B) * fa::padded_len(Lmax) * H * D;
   if (items >= (1ll << 31) || elems >= (1ll << 40)) return FA_ERR_INVALID_ARG;
-  if (static_cast<long long>(B) * H * fa::padded_len(L) >= (1ll << 31)) return FA_ERR_INVALID_ARG;
+  if (static_cast<long long>(B) * H * fa::padded_len(Lmax) >= (1ll << 31)) return FA_ERR_INVALID_ARG;
   return FA_OK;
+}
+
+fa_status check_shape(int B, int L, int H, int Hkv, int D, int dtype) {
+  return check_shape(B, L, L, H, Hkv, D, dtype);
 }
 
 }  // namespace
@@ -36,7 +42,18 @@ fa_status fa_fwd(const void* Q, const void* K, const void* V, void* O, float* LS
   if (st != FA_OK) return st;
   if (!ptr_ok(Q) || !ptr_ok(K) || !ptr_ok(V) || !ptr_ok(O) || !ptr_ok(LSE))
     return FA_ERR_INVALID_ARG;
-  return fa::run_fwd(Q, K, V, O, LSE, B, L, H, Hkv, D, causal, dtype,
+  return fa::run_fwd(Q, K, V, O, LSE, B, L, L, H, Hkv, D, causal, dtype,
+                     static_cast<cudaStream_t>(stream));
+}
+
+fa_status fa_fwd_kv(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int Lq,
+                    int Lk, int H, int Hkv, int D, int causal, int dtype, void* stream) {
+  fa_status st = check_shape(B, Lq, Lk, H, Hkv, D, dtype);
+  if (st != FA_OK) return st;
+  if (causal && Lk < Lq) return FA_ERR_INVALID_ARG;
+  if (!ptr_ok(Q) || !ptr_ok(K) || !ptr_ok(V) || !ptr_ok(O) || !ptr_ok(LSE))
+    return FA_ERR_INVALID_ARG;
+  return fa::run_fwd(Q, K, V, O, LSE, B, Lq, Lk, H, Hkv, D, causal, dtype,
                      static_cast<cudaStream_t>(stream));
 }
 
@@ -65,8 +82,23 @@ fa_status fa_bwd(const void* Q, const void* K, const void* V, const void* O, con
   if (!ptr_ok(Q) || !ptr_ok(K) || !ptr_ok(V) || !ptr_ok(dO) || !ptr_ok(LSE) || !ptr_ok(Delta) ||
       !ptr_ok(dQ) || !ptr_ok(dK) || !ptr_ok(dV) || !ptr_ok(dq_accum))
     return FA_ERR_INVALID_ARG;
-  return fa::run_bwd(Q, K, V, dO, LSE, Delta, dQ, dK, dV, dq_accum, zero_accum, B, L, H, Hkv, D,
+  return fa::run_bwd(Q, K, V, dO, LSE, Delta, dQ, dK, dV, dq_accum, zero_accum, B, L, L, H, Hkv, D,
                      causal, dtype, static_cast<cudaStream_t>(stream));
+}
+
+fa_status fa_bwd_kv(const void* Q, const void* K, const void* V, const void* O, const void* dO,
+                    const float* LSE, const float* Delta, void* dQ, void* dK, void* dV,
+                    float* dq_accum, int zero_accum, int B, int Lq, int Lk, int H, int Hkv, int D,
+                    int causal, int dtype, void* stream) {
+  (void)O;
+  fa_status st = check_shape(B, Lq, Lk, H, Hkv, D, dtype);
+  if (st != FA_OK) return st;
+  if (causal && Lk < Lq) return FA_ERR_INVALID_ARG;
+  if (!ptr_ok(Q) || !ptr_ok(K) || !ptr_ok(V) || !ptr_ok(dO) || !ptr_ok(LSE) || !ptr_ok(Delta) ||
+      !ptr_ok(dQ) || !ptr_ok(dK) || !ptr_ok(dV) || !ptr_ok(dq_accum))
+    return FA_ERR_INVALID_ARG;
+  return fa::run_bwd(Q, K, V, dO, LSE, Delta, dQ, dK, dV, dq_accum, zero_accum, B, Lq, Lk, H, Hkv,
+                     D, causal, dtype, static_cast<cudaStream_t>(stream));
 }
 
 fa_status fa_bwd_main(const void* Q, const void* K, const void* V, const void* dO,
@@ -78,7 +110,7 @@ fa_status fa_bwd_main(const void* Q, const void* K, const void* V, const void* d
   if (!ptr_ok(Q) || !ptr_ok(K) || !ptr_ok(V) || !ptr_ok(dO) || !ptr_ok(LSE) || !ptr_ok(Delta) ||
       !ptr_ok(dK) || !ptr_ok(dV) || !ptr_ok(dq_accum))
     return FA_ERR_INVALID_ARG;
-  return fa::run_bwd_main(Q, K, V, dO, LSE, Delta, dK, dV, dq_accum, zero_accum, B, L, H, Hkv, D,
+  return fa::run_bwd_main(Q, K, V, dO, LSE, Delta, dK, dV, dq_accum, zero_accum, B, L, L, H, Hkv, D,
                           causal, dtype, static_cast<cudaStream_t>(stream));
 }
 

@@ -37,17 +37,17 @@ fa_status run_bwd_prep(const void* O, const void* dO, float* Delta, float* dq_ac
 template <int D, bool BF16>
 static fa_status launch_bwd(const void* Q, const void* K, const void* V, const void* dO,
                             const float* LSE, const float* Delta, void* dK, void* dV,
-                            float* dq_accum, int zero_accum, int B, int L, int H, int Hkv,
-                            int causal, cudaStream_t s) {
+                            float* dq_accum, int zero_accum, int B, int Lq, int Lk, int H,
+                            int Hkv, int causal, cudaStream_t s) {
   using Ly = BwdLayout<D>;
-  const int Lpad = padded_len(L);
+  const int Lpad = padded_len(Lq);
   if (zero_accum &&
       cudaMemsetAsync(dq_accum, 0, static_cast<size_t>(B) * H * Lpad * D * sizeof(float), s) !=
           cudaSuccess)
     return FA_ERR_CUDA;
   CUtensorMap tq, tk, tv, tdo;
-  if (!make_bshd_map(&tq, Q, B, L, H, D, BF16) || !make_bshd_map(&tk, K, B, L, Hkv, D, BF16) ||
-      !make_bshd_map(&tv, V, B, L, Hkv, D, BF16) || !make_bshd_map(&tdo, dO, B, L, H, D, BF16))
+  if (!make_bshd_map(&tq, Q, B, Lq, H, D, BF16) || !make_bshd_map(&tk, K, B, Lk, Hkv, D, BF16) ||
+      !make_bshd_map(&tv, V, B, Lk, Hkv, D, BF16) || !make_bshd_map(&tdo, dO, B, Lq, H, D, BF16))
     return FA_ERR_CUDA;
   BwdParams p;
   p.LSE = LSE;
@@ -56,11 +56,14 @@ static fa_status launch_bwd(const void* Q, const void* K, const void* V, const v
   p.dK = dK;
   p.dV = dV;
   p.B = B;
-  p.L = L;
+  p.Lq = Lq;
+  p.Lk = Lk;
+  p.past = Lk - Lq;
   p.H = H;
   p.Hkv = Hkv;
   p.causal = causal ? 1 : 0;
-  p.n_kv = Lpad / 128;
+  p.n_kv = (Lk + 127) / 128;
+  p.n_q = Lpad / 128;
   p.Lpad = Lpad;
   p.n_items = B * Hkv * p.n_kv;
   p.scale = 1.f / sqrtf(static_cast<float>(D));
@@ -87,18 +90,18 @@ static fa_status launch_post(const float* dq_accum, void* dQ, int B, int L, int 
 
 fa_status run_bwd_main(const void* Q, const void* K, const void* V, const void* dO,
                        const float* LSE, const float* Delta, void* dK, void* dV, float* dq_accum,
-                       int zero_accum, int B, int L, int H, int Hkv, int D, int causal, int dtype,
-                       cudaStream_t s) {
+                       int zero_accum, int B, int Lq, int Lk, int H, int Hkv, int D, int causal,
+                       int dtype, cudaStream_t s) {
   const bool bf16 = dtype == FA_BF16;
   if (D == 64)
     return bf16 ? launch_bwd<64, true>(Q, K, V, dO, LSE, Delta, dK, dV, dq_accum, zero_accum, B,
-                                       L, H, Hkv, causal, s)
+                                       Lq, Lk, H, Hkv, causal, s)
                 : launch_bwd<64, false>(Q, K, V, dO, LSE, Delta, dK, dV, dq_accum, zero_accum, B,
-                                        L, H, Hkv, causal, s);
-  return bf16 ? launch_bwd<128, true>(Q, K, V, dO, LSE, Delta, dK, dV, dq_accum, zero_accum, B, L,
-                                      H, Hkv, causal, s)
+                                        Lq, Lk, H, Hkv, causal, s);
+  return bf16 ? launch_bwd<128, true>(Q, K, V, dO, LSE, Delta, dK, dV, dq_accum, zero_accum, B,
+                                      Lq, Lk, H, Hkv, causal, s)
               : launch_bwd<128, false>(Q, K, V, dO, LSE, Delta, dK, dV, dq_accum, zero_accum, B,
-                                       L, H, Hkv, causal, s);
+                                       Lq, Lk, H, Hkv, causal, s);
 }
 
 fa_status run_bwd_post(const float* dq_accum, void* dQ, int B, int L, int H, int D, int dtype,
@@ -113,12 +116,12 @@ fa_status run_bwd_post(const float* dq_accum, void* dQ, int B, int L, int H, int
 
 fa_status run_bwd(const void* Q, const void* K, const void* V, const void* dO, const float* LSE,
                   const float* Delta, void* dQ, void* dK, void* dV, float* dq_accum,
-                  int zero_accum, int B, int L, int H, int Hkv, int D, int causal, int dtype,
-                  cudaStream_t s) {
-  fa_status st = run_bwd_main(Q, K, V, dO, LSE, Delta, dK, dV, dq_accum, zero_accum, B, L, H, Hkv,
-                              D, causal, dtype, s);
+                  int zero_accum, int B, int Lq, int Lk, int H, int Hkv, int D, int causal,
+                  int dtype, cudaStream_t s) {
+  fa_status st = run_bwd_main(Q, K, V, dO, LSE, Delta, dK, dV, dq_accum, zero_accum, B, Lq, Lk, H,
+                              Hkv, D, causal, dtype, s);
   if (st != FA_OK) return st;
-  return run_bwd_post(dq_accum, dQ, B, L, H, D, dtype, s);
+  return run_bwd_post(dq_accum, dQ, B, Lq, H, D, dtype, s);
 }
 
 unsigned int bwd_read_error(cudaStream_t s) { return read_and_clear_error(s); }
@@ -164,7 +167,8 @@ fa_status run_bwd_noalloc(const void* Q, const void* K, const void* V, const voi
   if (st != FA_OK) return st;
   // The array keeps the previous call's sums: clear the part this call uses.
   if (cudaMemsetAsync(acc, 0, need, s) != cudaSuccess) return FA_ERR_CUDA;
-  return run_bwd(Q, K, V, dO, LSE, Delta, dQ, dK, dV, acc, 0, B, L, H, Hkv, D, causal, dtype, s);
+  return run_bwd(Q, K, V, dO, LSE, Delta, dQ, dK, dV, acc, 0, B, L, L, H, Hkv, D, causal, dtype,
+                 s);
 }
 
 }  // namespace fa

@@ -47,14 +47,16 @@
 namespace fa {
 
 struct BwdParams {
-  const float* LSE;    // [B, H, L]
-  const float* Delta;  // [B, H, L]
-  float* dq_accum;     // [B, H, D/4, Lpad, 4]
-  void* dK;            // [B, L, Hkv, D]
-  void* dV;            // [B, L, Hkv, D]
-  int B, L, H, Hkv, causal;
-  int n_kv;     // ceil(L / 128) (also the number of Q tiles)
-  int Lpad;     // n_kv * 128
+  const float* LSE;    // [B, H, Lq]
+  const float* Delta;  // [B, H, Lq]
+  float* dq_accum;     // [B, H, D/4, Lpad, 4], Lpad = n_q * 128
+  void* dK;            // [B, Lk, Hkv, D]
+  void* dV;            // [B, Lk, Hkv, D]
+  int B, Lq, Lk, H, Hkv, causal;
+  int past;     // Lk - Lq: query i sees keys j <= i + past under causal masking
+  int n_kv;     // ceil(Lk / 128) K/V tiles
+  int n_q;      // ceil(Lq / 128) Q tiles
+  int Lpad;     // n_q * 128
   int n_items;  // B * Hkv * n_kv
   float sl2;    // log2(e) / sqrt(D)
   float scale;  // 1 / sqrt(D)
@@ -107,15 +109,16 @@ __device__ __forceinline__ BwdItem bwd_decode(int item, const BwdParams& p) {
   const int bh = item / p.n_kv;
   it.b = bh / p.Hkv;
   it.hkv = bh - it.b * p.Hkv;
-  it.i0 = p.causal ? it.j : 0;
-  it.ntiles = (p.H / p.Hkv) * (p.n_kv - it.i0);
+  // causal: the first Q tile holding a query that sees key j*128
+  it.i0 = p.causal ? max(0, it.j * 128 - p.past) / 128 : 0;
+  it.ntiles = (p.H / p.Hkv) * (p.n_q - it.i0);
   return it;
 }
 
 // n-th (head, Q tile) pair of an item: heads of the group outer, tiles inner.
 __device__ __forceinline__ void bwd_tile(const BwdItem& it, const BwdParams& p, int n, int& h,
                                          int& i) {
-  const int per = p.n_kv - it.i0;
+  const int per = p.n_q - it.i0;
   const int g = n / per;
   i = it.i0 + (n - g * per);
   h = it.hkv * (p.H / p.Hkv) + g;
@@ -202,12 +205,12 @@ __global__ void __launch_bounds__(512, 1)
       if (!mbar_wait_warp(bar(Ly::B_QEMPTY + stage), phase ^ 1u, ab, err, 401)) { ok = false; break; }
       // LSE (pre-multiplied by log2 e) and Delta of the 128 query rows of tile i.
       float* st = stats + stage * 256;
-      const size_t row0 = (static_cast<size_t>(it.b) * p.H + h) * p.L;
+      const size_t row0 = (static_cast<size_t>(it.b) * p.H + h) * p.Lq;
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
         const int c = lane + 32 * u;
         const int q = i * 128 + c;
-        const bool in = q < p.L;
+        const bool in = q < p.Lq;
         st[c] = in ? p.LSE[row0 + q] * 1.4426950408889634f : 0.f;
         st[128 + c] = in ? p.Delta[row0 + q] : 0.f;
       }
@@ -337,9 +340,9 @@ __global__ void __launch_bounds__(512, 1)
         const float* st = stats + stage * 256 + cbase;
         const int q0 = i * 128 + cbase;
         // query columns [lo, hi) of this chunk are visible to key kr
-        int lo = 0, hi = min(32, p.L - q0);
-        if (kr >= p.L) hi = 0;
-        if (p.causal) lo = max(0, kr - q0);
+        int lo = 0, hi = min(32, p.Lq - q0);
+        if (kr >= p.Lk) hi = 0;
+        if (p.causal) lo = max(0, kr - p.past - q0);
         const bool full = (lo == 0 && hi == 32);
         uint32_t sv[32], dp[32];
         tmem_ld32(tS, sv);
@@ -393,7 +396,7 @@ __global__ void __launch_bounds__(512, 1)
       const float sc = hc == 0 ? p.scale : 1.f;
       const uint32_t tsrc = tmem + lane_off + (hc == 0 ? Ly::TM_DK : Ly::TM_DV);
       T* row = reinterpret_cast<T*>(dst_base) +
-               ((static_cast<size_t>(it.b) * p.L + kr) * p.Hkv + it.hkv) * D;
+               ((static_cast<size_t>(it.b) * p.Lk + kr) * p.Hkv + it.hkv) * D;
 #pragma unroll
       for (int cc = 0; cc < D / 32; ++cc) {
         uint32_t o[32];
@@ -403,7 +406,7 @@ __global__ void __launch_bounds__(512, 1)
 #pragma unroll
         for (int u = 0; u < 16; ++u)
           pk[u] = pack2<T>(__uint_as_float(o[2 * u]) * sc, __uint_as_float(o[2 * u + 1]) * sc);
-        if (kr < p.L) {
+        if (kr < p.Lk) {
           uint4* dst = reinterpret_cast<uint4*>(row + 32 * cc);
 #pragma unroll
           for (int u = 0; u < 4; ++u)
@@ -435,7 +438,7 @@ __global__ void __launch_bounds__(512, 1)
         // This half is in registers: release its columns before the atomics.
         tc_fence_before();
         mbar_arrive(bar(Ly::B_DQEMPTY + hq));
-        if (q < p.L) {
+        if (q < p.Lq) {
 #pragma unroll
           for (int c4 = 0; c4 < 16; ++c4)
             atomicAdd(acc + static_cast<size_t>(16 * hq + c4) * p.Lpad,

@@ -9,22 +9,24 @@ namespace fa {
 
 template <int D, bool BF16>
 static fa_status launch(const void* Q, const void* K, const void* V, void* O, float* LSE, int B,
-                        int L, int H, int Hkv, int causal, cudaStream_t s) {
+                        int Lq, int Lk, int H, int Hkv, int causal, cudaStream_t s) {
   using Ly = FwdLayout<D>;
   CUtensorMap tq, tk, tv;
-  if (!make_bshd_map(&tq, Q, B, L, H, D, BF16) || !make_bshd_map(&tk, K, B, L, Hkv, D, BF16) ||
-      !make_bshd_map(&tv, V, B, L, Hkv, D, BF16))
+  if (!make_bshd_map(&tq, Q, B, Lq, H, D, BF16) || !make_bshd_map(&tk, K, B, Lk, Hkv, D, BF16) ||
+      !make_bshd_map(&tv, V, B, Lk, Hkv, D, BF16))
     return FA_ERR_CUDA;
   FwdParams p;
   p.O = O;
   p.LSE = LSE;
   p.B = B;
-  p.L = L;
+  p.Lq = Lq;
+  p.Lk = Lk;
+  p.past = Lk - Lq;
   p.H = H;
   p.Hkv = Hkv;
   p.causal = causal ? 1 : 0;
-  p.n_kv = (L + 127) / 128;
-  p.n_qpairs = (L + 255) / 256;
+  p.n_kv = (Lk + 127) / 128;
+  p.n_qpairs = (Lq + 255) / 256;
   p.n_items = B * H * p.n_qpairs;
   p.sl2 = 1.4426950408889634f / sqrtf(static_cast<float>(D));
   auto kern = fa_fwd_kernel<D, BF16>;
@@ -36,15 +38,15 @@ static fa_status launch(const void* Q, const void* K, const void* V, void* O, fl
   return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
-fa_status run_fwd(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int L,
-                  int H, int Hkv, int D, int causal, int dtype, cudaStream_t s) {
+fa_status run_fwd(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int Lq,
+                  int Lk, int H, int Hkv, int D, int causal, int dtype, cudaStream_t s) {
   const bool bf16 = dtype == FA_BF16;
   if (D == 64) {
-    return bf16 ? launch<64, true>(Q, K, V, O, LSE, B, L, H, Hkv, causal, s)
-                : launch<64, false>(Q, K, V, O, LSE, B, L, H, Hkv, causal, s);
+    return bf16 ? launch<64, true>(Q, K, V, O, LSE, B, Lq, Lk, H, Hkv, causal, s)
+                : launch<64, false>(Q, K, V, O, LSE, B, Lq, Lk, H, Hkv, causal, s);
   }
-  return bf16 ? launch<128, true>(Q, K, V, O, LSE, B, L, H, Hkv, causal, s)
-              : launch<128, false>(Q, K, V, O, LSE, B, L, H, Hkv, causal, s);
+  return bf16 ? launch<128, true>(Q, K, V, O, LSE, B, Lq, Lk, H, Hkv, causal, s)
+              : launch<128, false>(Q, K, V, O, LSE, B, Lq, Lk, H, Hkv, causal, s);
 }
 
 unsigned int fwd_read_error(cudaStream_t s) { return read_and_clear_error(s); }

@@ -35,11 +35,12 @@
 namespace fa {
 
 struct FwdParams {
-  void* O;      // [B, L, H, D] fp16/bf16
-  float* LSE;   // [B, H, L] fp32, natural log
-  int B, L, H, Hkv, causal;
-  int n_kv;      // ceil(L / 128)
-  int n_qpairs;  // ceil(L / 256)
+  void* O;      // [B, Lq, H, D] fp16/bf16
+  float* LSE;   // [B, H, Lq] fp32, natural log
+  int B, Lq, Lk, H, Hkv, causal;
+  int past;      // Lk - Lq: causal offset (query i sees keys j <= i + past)
+  int n_kv;      // ceil(Lk / 128)
+  int n_qpairs;  // ceil(Lq / 256)
   int n_items;   // B * H * n_qpairs
   float sl2;     // log2(e) / sqrt(D)
 };
@@ -82,8 +83,8 @@ __device__ __forceinline__ FwdItem fwd_decode(int item, const FwdParams& p) {
 #pragma unroll
   for (int t = 0; t < 2; ++t) {
     const int lo = it.q0 + 128 * t;
-    if (lo >= p.L) it.n[t] = 0;
-    else it.n[t] = p.causal ? (lo / 128 + 1) : p.n_kv;
+    if (lo >= p.Lq) it.n[t] = 0;
+    else it.n[t] = p.causal ? min((lo + 127 + p.past) / 128 + 1, p.n_kv) : p.n_kv;
   }
   return it;
 }
@@ -340,10 +341,10 @@ __global__ void __launch_bounds__(320, 1)
         tmem_ld_wait32(sr + 64);
         tmem_ld_wait32(sr + 96);
         const int k0 = j * 128;
-        const bool need_mask = (k0 + 128 > p.L) || (p.causal && k0 + 127 > tile_lo);
+        const bool need_mask = (k0 + 128 > p.Lk) || (p.causal && k0 + 127 > tile_lo + p.past);
         float mx = -INFINITY;
         if (need_mask) {
-          const int lim = p.causal ? min(q + 1, p.L) : p.L;  // keys [0, lim) are visible
+          const int lim = p.causal ? min(q + p.past + 1, p.Lk) : p.Lk;  // keys [0, lim) visible
 #pragma unroll
           for (int c = 0; c < 128; ++c) {
             if (k0 + c >= lim) sr[c] = __float_as_uint(-INFINITY);
@@ -403,7 +404,7 @@ __global__ void __launch_bounds__(320, 1)
       ++o_cnt;
       tc_fence_after();
       const float inv = l > 0.f ? 1.f / l : 0.f;
-      T* orow = reinterpret_cast<T*>(p.O) + ((static_cast<size_t>(it.b) * p.L + q) * p.H + it.h) * D;
+      T* orow = reinterpret_cast<T*>(p.O) + ((static_cast<size_t>(it.b) * p.Lq + q) * p.H + it.h) * D;
 #pragma unroll
       for (int cc = 0; cc < D / 32; ++cc) {
         uint32_t o[32];
@@ -413,15 +414,15 @@ __global__ void __launch_bounds__(320, 1)
 #pragma unroll
         for (int i = 0; i < 16; ++i)
           pk[i] = pack2<T>(__uint_as_float(o[2 * i]) * inv, __uint_as_float(o[2 * i + 1]) * inv);
-        if (q < p.L) {
+        if (q < p.Lq) {
           uint4* dst = reinterpret_cast<uint4*>(orow + 32 * cc);
 #pragma unroll
           for (int i = 0; i < 4; ++i)
             dst[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
         }
       }
-      if (q < p.L)
-        p.LSE[(static_cast<size_t>(it.b) * p.H + it.h) * p.L + q] =
+      if (q < p.Lq)
+        p.LSE[(static_cast<size_t>(it.b) * p.H + it.h) * p.Lq + q] =
             (m * sl2 + __log2f(l)) * 0.6931471805599453f;
       tc_fence_before();
       mbar_arrive(bar(Ly::B_OEMPTY + t));

@@ -7,8 +7,8 @@
 
 namespace fa {
 
-fa_status run_fwd(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int L,
-                  int H, int Hkv, int D, int causal, int dtype, cudaStream_t s);
+fa_status run_fwd(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int Lq,
+                  int Lk, int H, int Hkv, int D, int causal, int dtype, cudaStream_t s);
 unsigned int fwd_read_error(cudaStream_t s);
 fa_status run_selftest_wait(unsigned long long limit_ns, cudaStream_t s);
 
@@ -16,12 +16,12 @@ fa_status run_bwd_prep(const void* O, const void* dO, float* Delta, float* dq_ac
                        int H, int D, int dtype, cudaStream_t s);
 fa_status run_bwd(const void* Q, const void* K, const void* V, const void* dO, const float* LSE,
                   const float* Delta, void* dQ, void* dK, void* dV, float* dq_accum,
-                  int zero_accum, int B, int L, int H, int Hkv, int D, int causal, int dtype,
-                  cudaStream_t s);
+                  int zero_accum, int B, int Lq, int Lk, int H, int Hkv, int D, int causal,
+                  int dtype, cudaStream_t s);
 fa_status run_bwd_main(const void* Q, const void* K, const void* V, const void* dO,
                        const float* LSE, const float* Delta, void* dK, void* dV, float* dq_accum,
-                       int zero_accum, int B, int L, int H, int Hkv, int D, int causal, int dtype,
-                       cudaStream_t s);
+                       int zero_accum, int B, int Lq, int Lk, int H, int Hkv, int D, int causal,
+                       int dtype, cudaStream_t s);
 fa_status run_bwd_post(const float* dq_accum, void* dQ, int B, int L, int H, int D, int dtype,
                        cudaStream_t s);
 unsigned int bwd_read_error(cudaStream_t s);
