@@ -44,19 +44,26 @@ WORKLOADS = {
     "b1_h32_l4096_d128": dict(B=1, L=4096, H=32, Hkv=32, D=128, dtype="fp16"),
     "b1_h32_l8192_d128": dict(B=1, L=8192, H=32, Hkv=32, D=128, dtype="fp16"),
     "b1_h32_l16384_d128": dict(B=1, L=16384, H=32, Hkv=32, D=128, dtype="fp16"),
+    # prefill of 1024 new queries against an 8192-position key/value sequence
+    "prefill_b8_h32_lq1024_lk8192_d128": dict(B=8, L=1024, Lk=8192, H=32, Hkv=32, D=128,
+                                              dtype="fp16"),
 }
 METRIC = "attention fwd/bwd TFLOP/s (fp16 B8 H32 L4096 D128) and % of GB300 TC peak"
 KERNEL_SOURCES = ["tiled_attention_fa_gb300/csrc/ptx.cuh", "tiled_attention_fa_gb300/csrc/common.cuh",
                   "tiled_attention_fa_gb300/csrc/fwd.cuh", "tiled_attention_fa_gb300/csrc/bwd.cuh"]
 
 
-def fwd_flops(B, H, L, D, causal):
-    f = 4.0 * B * H * L * L * D
-    return f / 2 if causal else f
+def fwd_flops(B, H, L, D, causal, Lk=None):
+    """4*B*H*Lq*Lk*D; causal counts the visible (query, key) pairs, i.e. half
+    the square for Lq == Lk and Lq*(Lk-Lq) + Lq^2/2 when the queries are the
+    last Lq of Lk positions."""
+    Lk = L if Lk is None else Lk
+    pairs = (L * (Lk - L) + L * L / 2.0) if causal else float(L) * Lk
+    return 4.0 * B * H * D * pairs
 
 
-def step_flops(B, H, L, D, causal):
-    return 3.5 * fwd_flops(B, H, L, D, causal)   # forward + 2.5x backward
+def step_flops(B, H, L, D, causal, Lk=None):
+    return 3.5 * fwd_flops(B, H, L, D, causal, Lk)   # forward + 2.5x backward
 
 
 def peaks():
@@ -233,9 +240,11 @@ def reference_arm(args):
 
 def config_dict(args, world):
     B, L, H, Hkv, D = WORK["B"], WORK["L"], WORK["H"], WORK["Hkv"], WORK["D"]
-    return {"workload": f"attention fwd+bwd B{B} H{H} Hkv{Hkv} L{L} D{D} {WORK['dtype']} "
+    Lk = WORK.get("Lk", L)
+    lens = f"L{L}" if Lk == L else f"Lq{L} Lk{Lk}"
+    return {"workload": f"attention fwd+bwd B{B} H{H} Hkv{Hkv} {lens} D{D} {WORK['dtype']} "
                         f"{'causal' if args.causal else 'non-causal'}",
-            "B": B, "L": L, "H": H, "Hkv": Hkv, "D": D, "causal": bool(args.causal),
+            "B": B, "L": L, "Lk": Lk, "H": H, "Hkv": Hkv, "D": D, "causal": bool(args.causal),
             "per_gpu_batch": B, "global_batch": B * world, "parallelism": f"replicas x{world}",
             "l2": ("inputs larger than L2 (Q, K, V, dO %d MB each)" % (B * L * H * D * 2 // 10**6)
                    if B * L * H * D * 2 > 129 * 10**6 else "inputs fit in L2 (no flush)")}
@@ -253,12 +262,13 @@ def ours_arm(args):
     _lib.load()  # fails loudly without the built library
 
     B, L, H, Hkv, D = WORK["B"], WORK["L"], WORK["H"], WORK["Hkv"], WORK["D"]
+    Lk = WORK.get("Lk", L)
     causal = bool(args.causal)
     dt = torch.float16 if WORK["dtype"] == "fp16" else torch.bfloat16
     g = torch.Generator(device=dev).manual_seed(replicas.replica_seed(1234, rank))
     q = torch.randn(B, L, H, D, device=dev, dtype=dt, generator=g)
-    k = torch.randn(B, L, Hkv, D, device=dev, dtype=dt, generator=g)
-    v = torch.randn(B, L, Hkv, D, device=dev, dtype=dt, generator=g)
+    k = torch.randn(B, Lk, Hkv, D, device=dev, dtype=dt, generator=g)
+    v = torch.randn(B, Lk, Hkv, D, device=dev, dtype=dt, generator=g)
     do = torch.randn(B, L, H, D, device=dev, dtype=dt, generator=g)
     o = torch.empty_like(q)
     lse = torch.empty(B, H, L, device=dev, dtype=torch.float32)
@@ -276,11 +286,17 @@ def ours_arm(args):
         fa.bwd_preprocess(o, do, delta=delta, dq_accum=acc, stream=stream)
         if ev:
             ev[2].record(stream)
-        fa.bwd_main(q, k, v, do, lse, delta, acc, causal, dk=dk, dv=dv, accum_zeroed=True,
-                    stream=stream)
-        if ev:
-            ev[3].record(stream)
-        fa.bwd_postprocess(acc, dq, stream=stream)
+        if Lk == L:
+            fa.bwd_main(q, k, v, do, lse, delta, acc, causal, dk=dk, dv=dv, accum_zeroed=True,
+                        stream=stream)
+            if ev:
+                ev[3].record(stream)
+            fa.bwd_postprocess(acc, dq, stream=stream)
+        else:  # fa_bwd_kv runs both stages; the post-process share is attributed to the main pass
+            fa.bwd(q, k, v, o, do, lse, delta, causal, dq=dq, dk=dk, dv=dv, dq_accum=acc,
+                   accum_zeroed=True, stream=stream)
+            if ev:
+                ev[3].record(stream)
         if ev:
             ev[4].record(stream)
 
@@ -308,7 +324,7 @@ def ours_arm(args):
 
     names = ["fa_fwd_kernel", "fa_bwd_prep_kernel", "fa_bwd_kernel", "fa_dq_convert_kernel"]
     kms = {n: statistics.mean(e[i].elapsed_time(e[i + 1]) for e in evs) for i, n in enumerate(names)}
-    f_fwd = fwd_flops(B, H, L, D, causal)
+    f_fwd = fwd_flops(B, H, L, D, causal, Lk)
     f_bwd = 2.5 * f_fwd
     Lpad = (L + 127) // 128 * 128
     prep_bytes = 2 * B * L * H * D * 2 + 4 * B * H * L + 4 * B * H * Lpad * D
@@ -337,12 +353,12 @@ def ours_arm(args):
                 "frac": ach / hbm, "peak_source": f"{src} copy bandwidth"}
     roof["traffic"] = recorded_traffic(dom)
 
-    value = replicas.aggregate_rate(step_flops(B, H, L, D, causal), world, ms_per_step * 1e-3) / 1e12
+    value = replicas.aggregate_rate(step_flops(B, H, L, D, causal, Lk), world, ms_per_step * 1e-3) / 1e12
 
     # ---- end to end through the public API with host buffers
     e2e = None
     if not args.no_e2e:
-        runner = fa.HostRunner(B, L, H, Hkv, D, dt, causal, dev)
+        runner = fa.HostRunner(B, L, H, Hkv, D, dt, causal, dev, Lk=Lk)
         hq, hk, hv, hdo = (x.cpu().pin_memory() for x in (q, k, v, do))
         runner.run(hq, hk, hv, hdo)
         torch.cuda.synchronize()
@@ -356,7 +372,7 @@ def ours_arm(args):
         s1.record(stream)
         torch.cuda.synchronize()
         ems = replicas.max_over_ranks(s0.elapsed_time(s1) / n_e2e, dev)
-        e2e = {"value": replicas.aggregate_rate(step_flops(B, H, L, D, causal), world, ems * 1e-3) / 1e12,
+        e2e = {"value": replicas.aggregate_rate(step_flops(B, H, L, D, causal, Lk), world, ems * 1e-3) / 1e12,
                "unit": "TFLOP/s", "h2d_bytes_per_step": runner.h2d_bytes(),
                "d2h_bytes_per_step": runner.d2h_bytes(), "ms_per_step": ems, "steps": n_e2e}
         del runner

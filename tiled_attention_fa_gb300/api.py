@@ -195,11 +195,13 @@ class HostRunner:
     once per shape and reused.
     """
 
-    def __init__(self, B, L, H, Hkv, D, dtype=torch.float16, causal=False, device="cuda"):
+    def __init__(self, B, L, H, Hkv, D, dtype=torch.float16, causal=False, device="cuda",
+                 Lk=None):
         self.causal = causal
         dev = torch.device(device)
+        Lk = L if Lk is None else Lk
         self.q = torch.empty(B, L, H, D, dtype=dtype, device=dev)
-        self.k = torch.empty(B, L, Hkv, D, dtype=dtype, device=dev)
+        self.k = torch.empty(B, Lk, Hkv, D, dtype=dtype, device=dev)
         self.v = torch.empty_like(self.k)
         self.do = torch.empty_like(self.q)
         self.o = torch.empty_like(self.q)
