@@ -35,7 +35,8 @@ typedef enum {
   FA_ERR_UNSUPPORTED = 2,    /* D or dtype outside the supported set */
   FA_ERR_CUDA = 3,           /* a CUDA runtime call or kernel launch failed */
   FA_ERR_DEVICE_TIMEOUT = 4, /* a kernel gave up a bounded wait (see fa_check_device_error) */
-  FA_ERR_SCRATCH_TOO_SMALL = 5 /* fa_bwd_noalloc: the problem needs more than its fixed scratch */
+  FA_ERR_SCRATCH_TOO_SMALL = 5 /* fa_bwd_noalloc's fixed scratch or fa_decode's workspace is
+                                  smaller than the problem needs; nothing was launched */
 } fa_status;
 
 typedef enum { FA_F16 = 0, FA_BF16 = 1 } fa_dtype;
@@ -67,6 +68,33 @@ fa_status fa_fwd(const void* Q, const void* K, const void* V, void* O, float* LS
  */
 fa_status fa_fwd_kv(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int Lq,
                     int Lk, int H, int Hkv, int D, int causal, int dtype, void* stream);
+
+/*
+ * Split-KV decoding: the forward of fa_fwd_kv (same result, layouts, masking
+ * rule and causal past_len = Lk - Lq) computed for few queries against many
+ * keys.  The keys of each (batch, K/V head) are cut into equal slices of
+ * 128-key tiles, one CTA per slice, sized so the slices fill the GPU; each
+ * slice yields a partial output and log-sum-exp in fp32, and a second kernel
+ * merges them: LSE = ln sum_s exp(LSE_s), O = sum_s exp(LSE_s - LSE) O_s.
+ * Page "TileLang性能分析报告：H100上FlashAttention吞吐量达1.2PFlops", section
+ * 生产环境部署建议 (item 2 names flash_decoding for inference; the slicing and
+ * merge are the plain reading of that name); the per-slice loop is the online
+ * softmax of page "使用 TileLang 在 AMD GPU 上快速开发高性能 Flash Attention",
+ * section K/V Tile 遍历与核心计算.
+ * The g = H / Hkv query heads of a K/V head and all Lq queries share one
+ * 128-row tile, so the call requires g * Lq <= 128 (FA_ERR_UNSUPPORTED
+ * otherwise; use fa_fwd_kv).  `workspace` is the caller's device buffer of
+ * `workspace_bytes` (16-byte aligned) holding the partials; it needs
+ * fa_decode_workspace_size(...) bytes, asked with the same sizes and with the
+ * device that will run the call current (the slice count depends on its SM
+ * count).  Smaller buffers return FA_ERR_SCRATCH_TOO_SMALL and launch nothing.
+ * Its contents need no initialisation and are unspecified afterwards; calls
+ * that overlap on the GPU must not share one workspace.
+ */
+size_t fa_decode_workspace_size(int B, int Lq, int Lk, int H, int Hkv, int D);
+fa_status fa_decode(const void* Q, const void* K, const void* V, void* O, float* LSE,
+                    void* workspace, size_t workspace_bytes, int B, int Lq, int Lk, int H, int Hkv,
+                    int D, int causal, int dtype, void* stream);
 
 /*
  * Backward preprocess: Delta[b, h, i] = sum_d O[b, i, h, d] * dO[b, i, h, d]

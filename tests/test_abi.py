@@ -81,3 +81,32 @@ def test_product_path_has_no_oracle_or_cpu_fallback():
             if f.endswith((".py", ".cu", ".cuh", ".h")):
                 src = open(os.path.join(dirpath, f), encoding="utf-8").read()
                 assert "import oracle" not in src and "from oracle" not in src, f
+
+
+def test_decode_argument_errors(lib):
+    """fa_decode rejects bad calls (and a short workspace) before any launch."""
+    big = 1 << 30
+    # (Q, K, V, O, LSE, ws, ws_bytes, B, Lq, Lk, H, Hkv, D, causal, dtype)
+    base = [FAKE] * 6 + [big, 2, 1, 4096, 32, 8, 128, 0, 1]
+
+    def call(**kw):
+        a = list(base)
+        names = ["Q", "K", "V", "O", "LSE", "ws", "ws_bytes", "B", "Lq", "Lk", "H", "Hkv", "D",
+                 "causal", "dtype"]
+        for key, val in kw.items():
+            a[names.index(key)] = val
+        return lib.fa_decode(*a, None)
+
+    assert call(ws=None) == _lib.FA_ERR_INVALID_ARG
+    assert call(ws=FAKE + 4) == _lib.FA_ERR_INVALID_ARG
+    assert call(Q=None) == _lib.FA_ERR_INVALID_ARG
+    assert call(H=30) == _lib.FA_ERR_INVALID_ARG             # H % Hkv != 0
+    assert call(D=96) == _lib.FA_ERR_UNSUPPORTED
+    assert call(Lq=33) == _lib.FA_ERR_UNSUPPORTED           # g * Lq = 132 > 128 packed rows
+    assert call(Lq=8, Lk=4, causal=1) == _lib.FA_ERR_INVALID_ARG  # causal needs Lk >= Lq
+    assert call(ws_bytes=0) == _lib.FA_ERR_SCRATCH_TOO_SMALL
+    need = lib.fa_decode_workspace_size(2, 1, 4096, 32, 8, 128)
+    assert need >= 2 * 32 * 1 * 129 * 4                      # one slice at least
+    assert call(ws_bytes=need - 1) == _lib.FA_ERR_SCRATCH_TOO_SMALL
+    assert lib.fa_decode_workspace_size(0, 1, 4096, 32, 8, 128) == 0
+    assert lib.fa_decode_workspace_size(2, 1, 4096, 32, 8, 80) == 0

@@ -15,9 +15,11 @@ from .api import (  # noqa: F401
     bwd_postprocess,
     bwd_preprocess,
     check_device_error,
+    decode,
+    decode_workspace_size,
     fwd,
     workspace_size,
 )
 
 __all__ = ["fwd", "bwd_preprocess", "bwd", "attention_backward", "bwd_main", "bwd_postprocess", "workspace_size",
-           "alloc_workspace", "check_device_error", "HostRunner"]
+           "alloc_workspace", "check_device_error", "HostRunner", "decode", "decode_workspace_size"]

@@ -69,6 +69,40 @@ def fwd(q, k, v, causal: bool = False, out=None, lse=None, stream=None):
     return out, lse
 
 
+def decode_workspace_size(B: int, Lq: int, Lk: int, H: int, Hkv: int, D: int) -> int:
+    """Bytes of the partial-result workspace ``decode`` needs on the current device."""
+    return int(_lib.load().fa_decode_workspace_size(B, Lq, Lk, H, Hkv, D))
+
+
+def decode(q, k, v, causal: bool = False, out=None, lse=None, workspace=None, stream=None):
+    """Split-KV decoding: O, LSE = attention(Q, K, V) for few queries against
+    many keys.  q [B, Lq, H, D]; k, v [B, Lk, Hkv, D] with (H / Hkv) * Lq <= 128.
+    Same result and masking rule as ``fwd``.  ``workspace`` (a CUDA byte
+    tensor of at least ``decode_workspace_size`` bytes) is allocated when not
+    given."""
+    B, Lq, H, D = q.shape
+    Lk, Hkv = k.shape[1], k.shape[2]
+    _need(q, "q")
+    _need(k, "k", (B, Lk, Hkv, D), q.dtype)
+    _need(v, "v", (B, Lk, Hkv, D), q.dtype)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty(B, H, Lq, device=q.device, dtype=torch.float32)
+    _need(out, "out", q.shape, q.dtype)
+    _need(lse, "lse", (B, H, Lq), torch.float32)
+    if workspace is None:
+        workspace = torch.empty(max(decode_workspace_size(B, Lq, Lk, H, Hkv, D), 16),
+                                device=q.device, dtype=torch.uint8)
+    _need(workspace, "workspace")
+    nbytes = workspace.numel() * workspace.element_size()
+    st = _lib.load().fa_decode(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                               lse.data_ptr(), workspace.data_ptr(), nbytes, B, Lq, Lk, H, Hkv, D,
+                               int(bool(causal)), _dtype_code(q), _stream(stream))
+    _lib.check("fa_decode", st)
+    return out, lse
+
+
 def workspace_size(B: int, L: int, H: int, D: int) -> int:
     """Bytes of the fp32 dQ accumulator the backward needs."""
     return int(_lib.load().fa_bwd_workspace_size(B, L, H, D))

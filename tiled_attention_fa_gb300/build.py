@@ -21,7 +21,7 @@ CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(ROOT, "_build")
 LIB_NAME = "libfa_gb300.so"
 LIB_PATH = os.path.join(HERE, LIB_NAME)
-UNITS = ["api.cu", "fwd.cu", "bwd.cu"]
+UNITS = ["api.cu", "fwd.cu", "bwd.cu", "decode.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

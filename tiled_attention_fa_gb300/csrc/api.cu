@@ -136,13 +136,36 @@ fa_status fa_bwd_noalloc(const void* Q, const void* K, const void* V, const void
                              static_cast<cudaStream_t>(stream));
 }
 
+size_t fa_decode_workspace_size(int B, int Lq, int Lk, int H, int Hkv, int D) {
+  if (B < 1 || Lq < 1 || Lk < 1 || H < 1 || Hkv < 1 || H % Hkv != 0 || (D != 64 && D != 128))
+    return 0;
+  return fa::decode_workspace_size(B, Lq, Lk, H, Hkv, D);
+}
+
+fa_status fa_decode(const void* Q, const void* K, const void* V, void* O, float* LSE,
+                    void* workspace, size_t workspace_bytes, int B, int Lq, int Lk, int H, int Hkv,
+                    int D, int causal, int dtype, void* stream) {
+  fa_status st = check_shape(B, Lq, Lk, H, Hkv, D, dtype);
+  if (st != FA_OK) return st;
+  if (causal && Lk < Lq) return FA_ERR_INVALID_ARG;
+  if (static_cast<long long>(H / Hkv) * Lq > 128) return FA_ERR_UNSUPPORTED;
+  if (!ptr_ok(Q) || !ptr_ok(K) || !ptr_ok(V) || !ptr_ok(O) || !ptr_ok(LSE) || !ptr_ok(workspace))
+    return FA_ERR_INVALID_ARG;
+  return fa::run_decode(Q, K, V, O, LSE, workspace, workspace_bytes, B, Lq, Lk, H, Hkv, D, causal,
+                        dtype, static_cast<cudaStream_t>(stream));
+}
+
 fa_status fa_check_device_error(void* stream) {
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  const unsigned int a = fa::fwd_read_error(s);
-  const unsigned int b = fa::bwd_read_error(s);
-  if (a == 0xFFFFFFFFu || b == 0xFFFFFFFFu) return FA_ERR_CUDA;
-  if (a || b) {
-    g_last_site = a ? a : b;
+  const unsigned int words[3] = {fa::fwd_read_error(s), fa::bwd_read_error(s),
+                                 fa::decode_read_error(s)};
+  unsigned int site = 0;
+  for (unsigned int w : words) {
+    if (w == 0xFFFFFFFFu) return FA_ERR_CUDA;
+    if (w && !site) site = w;
+  }
+  if (site) {
+    g_last_site = site;
     return FA_ERR_DEVICE_TIMEOUT;
   }
   return FA_OK;
@@ -164,7 +187,8 @@ const char* fa_status_string(fa_status s) {
     case FA_ERR_CUDA: return "CUDA runtime or launch error";
     case FA_ERR_DEVICE_TIMEOUT: return "a kernel gave up a bounded wait";
     case FA_ERR_SCRATCH_TOO_SMALL:
-      return "problem needs more dQ scratch than fa_bwd_noalloc's fixed array holds";
+      return "scratch too small: the problem needs more than fa_bwd_noalloc's fixed array or "
+             "the fa_decode workspace given";
   }
   return "unknown status";
 }

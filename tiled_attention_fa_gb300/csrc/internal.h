@@ -30,6 +30,19 @@ fa_status run_bwd_noalloc(const void* Q, const void* K, const void* V, const voi
                           int B, int L, int H, int Hkv, int D, int causal, int dtype,
                           cudaStream_t s);
 
+// Split-KV decoding (decode.cu).
+struct DecodePlan {
+  int nsplit;  // key slices per (batch, K/V head)
+  int tps;     // 128-key tiles per slice
+  int n_kv;    // 128-key tiles in all
+};
+DecodePlan decode_plan(int B, int Lq, int Lk, int H, int Hkv, int sms);
+size_t decode_workspace_size(int B, int Lq, int Lk, int H, int Hkv, int D);
+fa_status run_decode(const void* Q, const void* K, const void* V, void* O, float* LSE, void* ws,
+                     size_t ws_bytes, int B, int Lq, int Lk, int H, int Hkv, int D, int causal,
+                     int dtype, cudaStream_t s);
+unsigned int decode_read_error(cudaStream_t s);
+
 inline int padded_len(int L) { return (L + 127) / 128 * 128; }
 
 }  // namespace fa

@@ -42,6 +42,22 @@ def make_qkv(B: int, L: int, H: int, Hkv: int, D: int, dtype="fp16",
     return q, k, v, do
 
 
+def make_qkv_kv(B: int, Lq: int, Lk: int, H: int, Hkv: int, D: int, dtype="fp16",
+                seed: int = 0, with_do: bool = False):
+    """Like ``make_qkv`` with Lq query positions and Lk key positions (same
+    draw order: Q, K, V, then dO)."""
+    g = torch.Generator(device="cpu")
+    g.manual_seed(int(seed))
+    dt = storage_dtype(dtype)
+    q = torch.randn(B, Lq, H, D, generator=g, dtype=torch.float32).to(dt)
+    k = torch.randn(B, Lk, Hkv, D, generator=g, dtype=torch.float32).to(dt)
+    v = torch.randn(B, Lk, Hkv, D, generator=g, dtype=torch.float32).to(dt)
+    do = None
+    if with_do:
+        do = torch.randn(B, Lq, H, D, generator=g, dtype=torch.float32).to(dt)
+    return q, k, v, do
+
+
 def make_unit(L: int, D: int, dtype="fp16", seed: int = 0, group: int = 1):
     """One (batch, kv-head) unit with ``group`` query heads: shapes [1, L, group, D]
     for Q/dO and [1, L, 1, D] for K/V.  Used for small, fast cases."""
