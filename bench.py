@@ -47,10 +47,19 @@ WORKLOADS = {
     # prefill of 1024 new queries against an 8192-position key/value sequence
     "prefill_b8_h32_lq1024_lk8192_d128": dict(B=8, L=1024, Lk=8192, H=32, Hkv=32, D=128,
                                               dtype="fp16"),
+    # split-KV decoding (forward only): few new queries against a long key/value sequence
+    "decode_b16_h32_hkv8_lq1_lk16384_d128_bf16": dict(mode="decode", B=16, L=1, Lk=16384, H=32,
+                                                      Hkv=8, D=128, dtype="bf16"),
+    "decode_b1_h32_hkv8_lq1_lk131072_d128_bf16": dict(mode="decode", B=1, L=1, Lk=131072, H=32,
+                                                      Hkv=8, D=128, dtype="bf16"),
+    "decode_b8_h32_hkv8_lq4_lk32768_d128_bf16": dict(mode="decode", B=8, L=4, Lk=32768, H=32,
+                                                     Hkv=8, D=128, dtype="bf16"),
 }
 METRIC = "attention fwd/bwd TFLOP/s (fp16 B8 H32 L4096 D128) and % of GB300 TC peak"
+DECODE_METRIC = "attention split-KV decode GB/s (Q, K, V read + O, LSE written)"
 KERNEL_SOURCES = ["tiled_attention_fa_gb300/csrc/ptx.cuh", "tiled_attention_fa_gb300/csrc/common.cuh",
-                  "tiled_attention_fa_gb300/csrc/fwd.cuh", "tiled_attention_fa_gb300/csrc/bwd.cuh"]
+                  "tiled_attention_fa_gb300/csrc/fwd.cuh", "tiled_attention_fa_gb300/csrc/bwd.cuh",
+                  "tiled_attention_fa_gb300/csrc/decode.cuh"]
 
 
 def fwd_flops(B, H, L, D, causal, Lk=None):
@@ -64,6 +73,15 @@ def fwd_flops(B, H, L, D, causal, Lk=None):
 
 def step_flops(B, H, L, D, causal, Lk=None):
     return 3.5 * fwd_flops(B, H, L, D, causal, Lk)   # forward + 2.5x backward
+
+
+def decode_bytes(B, Lq, Lk, H, Hkv, D, esize=2):
+    """Bytes decoding must move: Q, K, V read once, O and LSE written once."""
+    return esize * (2 * B * Lq * H * D + 2 * B * Lk * Hkv * D) + 4 * B * H * Lq
+
+
+def is_decode():
+    return WORK.get("mode") == "decode"
 
 
 def peaks():
@@ -215,6 +233,8 @@ def reference_arm(args):
     world, rank, _ = dist_setup()
     if rank != 0:
         return 0
+    if is_decode():
+        return decode_reference_arm(args, world)
     L, D = WORK["L"], WORK["D"]
     qs, ks, vs, dos = cpu_unit_inputs()
     flops_unit = step_flops(1, 1, L, D, args.causal)
@@ -251,6 +271,8 @@ def config_dict(args, world):
 
 
 def ours_arm(args):
+    if is_decode():
+        return decode_arm(args)
     import torch
     import tiled_attention_fa_gb300 as fa
     from tiled_attention_fa_gb300 import _lib, replicas
@@ -397,6 +419,197 @@ def ours_arm(args):
                              "source": src},
             "kernels": kernels, "roofline": roof, "clocks": clocks, "e2e": e2e,
             "cpu_baseline": cpu, "gpu_launches": 4 * args.steps,
+        }
+        print(json.dumps(out), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+# --------------------------------------------------------------------- decoding
+
+def decode_config(args, world):
+    B, Lq, Lk, H, Hkv, D = (WORK[x] for x in ("B", "L", "Lk", "H", "Hkv", "D"))
+    kv = 2 * B * Lk * Hkv * D * 2
+    return {"workload": f"attention split-KV decode B{B} H{H} Hkv{Hkv} Lq{Lq} Lk{Lk} D{D} "
+                        f"{WORK['dtype']} {'causal' if args.causal else 'non-causal'}",
+            "B": B, "Lq": Lq, "Lk": Lk, "H": H, "Hkv": Hkv, "D": D, "causal": bool(args.causal),
+            "per_gpu_batch": B, "global_batch": B * world, "parallelism": f"replicas x{world}",
+            "l2": (f"inputs larger than L2 (K and V {kv // 10**6} MB)" if kv > 129 * 10**6
+                   else "inputs fit in L2 (no flush)")}
+
+
+def time_oracle_groups(q, k, v, causal, n_groups, budget_s):
+    """Oracle forward of whole (batch, K/V head) groups (its g query heads,
+    all Lq queries) until ``n_groups`` or ``budget_s``; returns (groups, s)."""
+    from oracle import fa_oracle as orc
+    H, Hkv = q.shape[2], k.shape[2]
+    g = H // Hkv
+    done, t0 = 0, time.perf_counter()
+    for u in range(n_groups):
+        hk = u % Hkv
+        for h in range(hk * g, (hk + 1) * g):
+            orc.unit_forward(q[0, :, h], k[0, :, hk], v[0, :, hk], causal)
+        done += 1
+        if time.perf_counter() - t0 > budget_s:
+            break
+    return done, time.perf_counter() - t0
+
+
+def decode_group_inputs(seed=0):
+    """One batch entry of the decode workload as float64 host arrays."""
+    from tiled_attention_fa_gb300.inputs import make_qkv_kv
+    q, k, v, _ = make_qkv_kv(1, WORK["L"], WORK["Lk"], WORK["H"], WORK["Hkv"], WORK["D"],
+                             WORK["dtype"], seed=seed)
+    return tuple(t.double().numpy() for t in (q, k, v))
+
+
+def group_bytes():
+    Lq, Lk, H, Hkv, D = (WORK[x] for x in ("L", "Lk", "H", "Hkv", "D"))
+    return decode_bytes(1, Lq, Lk, H, Hkv, D) / Hkv
+
+
+def decode_reference_arm(args, world):
+    qs, ks, vs = decode_group_inputs()
+    time_oracle_groups(qs, ks, vs, args.causal, args.warmup, 1e9)
+    n, secs = time_oracle_groups(qs, ks, vs, args.causal, args.steps, 1e9)
+    value = n * group_bytes() / secs / 1e9
+    sample = (f"oracle fp64 forward of one (batch, K/V head) group ({WORK['H'] // WORK['Hkv']} "
+              f"query heads x Lq={WORK['L']}, Lk={WORK['Lk']}) per step, {n} steps")
+    out = {
+        "impl": "reference", "metric": DECODE_METRIC, "value": value, "unit": "GB/s",
+        "n_gpus": world, "steps": n, "warmup": args.warmup, "ms_per_step": secs / n * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": decode_config(args, world),
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": blas_threads(), "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(out), flush=True)
+    return 0
+
+
+def decode_arm(args):
+    import torch
+    import tiled_attention_fa_gb300 as fa
+    from tiled_attention_fa_gb300 import _lib, replicas
+
+    world, rank, local = dist_setup()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    replicas.init("nccl", dev)
+    _lib.load()  # fails loudly without the built library
+
+    B, Lq, Lk, H, Hkv, D = (WORK[x] for x in ("B", "L", "Lk", "H", "Hkv", "D"))
+    causal = bool(args.causal)
+    dt = torch.float16 if WORK["dtype"] == "fp16" else torch.bfloat16
+    g = torch.Generator(device=dev).manual_seed(replicas.replica_seed(4321, rank))
+    q = torch.randn(B, Lq, H, D, device=dev, dtype=dt, generator=g)
+    k = torch.randn(B, Lk, Hkv, D, device=dev, dtype=dt, generator=g)
+    v = torch.randn(B, Lk, Hkv, D, device=dev, dtype=dt, generator=g)
+    o = torch.empty_like(q)
+    lse = torch.empty(B, H, Lq, device=dev, dtype=torch.float32)
+    ws = fa.alloc_decode_workspace(B, Lq, Lk, H, Hkv, D, dev)
+    kv_bytes = 2 * k.numel() * k.element_size()
+    # Between timed steps an L2-sized buffer is rewritten when K/V would fit in L2.
+    flush = None if kv_bytes > 129 * 10**6 else torch.empty(256 << 20, device=dev, dtype=torch.uint8)
+    stream = torch.cuda.current_stream()
+
+    def step(ev=None):
+        if flush is not None:
+            flush.zero_()
+        if ev:
+            ev[0].record(stream)
+        fa.decode_slices(q, k, v, ws, causal, stream=stream)
+        if ev:
+            ev[1].record(stream)
+        fa.decode_merge(ws, o, lse, Lk, Hkv, stream=stream)
+        if ev:
+            ev[2].record(stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    fa.check_device_error()
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    sampler = ClockSampler(local, enabled=not args.no_clocks)
+    replicas.barrier()
+    torch.cuda.synchronize()
+    sampler.start()
+    t_start.record(stream)
+    for i in range(args.steps):
+        step(evs[i])
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    replicas.barrier()
+    clocks = sampler.stop()
+    fa.check_device_error()
+    if flush is None:
+        ms = t_start.elapsed_time(t_end) / args.steps
+    else:  # the L2 flush between steps is not part of a step
+        ms = statistics.mean(e[0].elapsed_time(e[2]) for e in evs)
+    ms_per_step = replicas.max_over_ranks(ms, dev)
+    kms = {"fa_decode_kernel": statistics.mean(e[0].elapsed_time(e[1]) for e in evs),
+           "fa_decode_combine_kernel": statistics.mean(e[1].elapsed_time(e[2]) for e in evs)}
+    alg = decode_bytes(B, Lq, Lk, H, Hkv, D)
+    part = fa.decode_workspace_size(B, Lq, Lk, H, Hkv, D)
+    slice_bytes = kv_bytes + q.numel() * q.element_size() + part
+    merge_bytes = part + o.numel() * o.element_size() + lse.numel() * 4
+    _, _, hbm, src = peaks()
+    kernels = {
+        "fa_decode_kernel": {"ms": kms["fa_decode_kernel"],
+                             "gbs": slice_bytes / kms["fa_decode_kernel"] / 1e6},
+        "fa_decode_combine_kernel": {"ms": kms["fa_decode_combine_kernel"],
+                                     "gbs": merge_bytes / kms["fa_decode_combine_kernel"] / 1e6},
+    }
+    ach = kernels["fa_decode_kernel"]["gbs"]
+    roof = {"kernel": "fa_decode_kernel", "bound": "hbm", "achieved": ach, "peak": hbm,
+            "unit": "GB/s", "frac": ach / hbm, "peak_source": f"{src} copy bandwidth",
+            "traffic": recorded_traffic("fa_decode_kernel"),
+            "algorithmic_bytes_per_launch": slice_bytes}
+    value = replicas.aggregate_rate(alg, world, ms_per_step * 1e-3) / 1e9
+    tflops = fwd_flops(B, H, Lq, D, causal, Lk) / (ms_per_step * 1e-3) / 1e12
+
+    e2e = None
+    if not args.no_e2e:
+        runner = fa.DecodeHostRunner(B, Lq, Lk, H, Hkv, D, dt, causal, dev)
+        hq, hk, hv = (x.cpu().pin_memory() for x in (q, k, v))
+        runner.run(hq, hk, hv)
+        torch.cuda.synchronize()
+        n_e2e = max(3, min(args.steps, 10))
+        s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        replicas.barrier()
+        torch.cuda.synchronize()
+        s0.record(stream)
+        for _ in range(n_e2e):
+            runner.run(hq, hk, hv, stream=stream)
+        s1.record(stream)
+        torch.cuda.synchronize()
+        ems = replicas.max_over_ranks(s0.elapsed_time(s1) / n_e2e, dev)
+        e2e = {"value": replicas.aggregate_rate(alg, world, ems * 1e-3) / 1e9, "unit": "GB/s",
+               "h2d_bytes_per_step": runner.h2d_bytes(), "d2h_bytes_per_step": runner.d2h_bytes(),
+               "ms_per_step": ems, "steps": n_e2e}
+        del runner
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        qs, ks, vs = decode_group_inputs()
+        n, secs = time_oracle_groups(qs, ks, vs, causal, 100000, args.cpu_budget)
+        cpu = {"value": n * group_bytes() / secs / 1e9, "unit": "GB/s", "cores": blas_threads(),
+               "kind": "oracle",
+               "sample": f"{n} (batch, K/V head) group(s) of the workload, forward in fp64 "
+                         f"({secs:.1f} s)"}
+
+    if rank == 0:
+        out = {
+            "metric": DECODE_METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": WORK["dtype"], "data": "synthetic", "config": decode_config(args, world),
+            "tflops": tflops, "kernels": kernels, "roofline": roof, "clocks": clocks, "e2e": e2e,
+            "cpu_baseline": cpu, "gpu_launches": 2 * args.steps,
         }
         print(json.dumps(out), flush=True)
     if world > 1:

@@ -97,6 +97,19 @@ fa_status fa_decode(const void* Q, const void* K, const void* V, void* O, float*
                     int D, int causal, int dtype, void* stream);
 
 /*
+ * The two stages fa_decode runs, for callers that schedule or time them
+ * apart: fa_decode_slices writes every slice's partial O and LSE into the
+ * workspace; fa_decode_merge reads them and writes O and LSE.  Give both the
+ * same sizes and run them on the same device, so that they derive the same
+ * slice plan; the merge must run after the slices on the stream.
+ */
+fa_status fa_decode_slices(const void* Q, const void* K, const void* V, void* workspace,
+                           size_t workspace_bytes, int B, int Lq, int Lk, int H, int Hkv, int D,
+                           int causal, int dtype, void* stream);
+fa_status fa_decode_merge(const void* workspace, size_t workspace_bytes, void* O, float* LSE, int B,
+                          int Lq, int Lk, int H, int Hkv, int D, int dtype, void* stream);
+
+/*
  * Backward preprocess: Delta[b, h, i] = sum_d O[b, i, h, d] * dO[b, i, h, d]
  * (fp32 accumulation), the per-row term of the softmax gradient.  Page
  * "TileLang与机器学习训练：反向传播算子优化案例", section 算子拆分与流水线设计

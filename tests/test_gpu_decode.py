@@ -106,3 +106,17 @@ def test_decode_long_b1_lk131072(cuda_lib):
         assert_close(to64(o)[0, :, h], ro, name=f"O[h={h}]")
         assert_close(to64(lse)[0, h], rl, rtol=0, atol=LSE_ATOL, name=f"LSE[h={h}]")
     assert np.isfinite(to64(o)).all()
+
+
+def test_two_stage_calls_match_decode(cuda_lib):
+    """fa_decode_slices then fa_decode_merge give fa_decode's result bit for bit."""
+    q, k, v, _ = make_qkv_kv(2, 2, 5000, 16, 4, 64, "fp16", 11)
+    qd, kd, vd = (x.cuda() for x in (q, k, v))
+    o1, l1 = fa.decode(qd, kd, vd, True)
+    ws = fa.alloc_decode_workspace(2, 2, 5000, 16, 4, 64, qd.device)
+    o2, l2 = torch.empty_like(o1), torch.empty_like(l1)
+    fa.decode_slices(qd, kd, vd, ws, True)
+    fa.decode_merge(ws, o2, l2, 5000, 4)
+    torch.cuda.synchronize()
+    fa.check_device_error()
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)

@@ -7,6 +7,7 @@ package only marshals torch tensors into it.  Build the library with
 """
 
 from .api import (  # noqa: F401
+    DecodeHostRunner,
     HostRunner,
     alloc_workspace,
     attention_backward,
@@ -15,11 +16,15 @@ from .api import (  # noqa: F401
     bwd_postprocess,
     bwd_preprocess,
     check_device_error,
+    alloc_decode_workspace,
     decode,
+    decode_merge,
+    decode_slices,
     decode_workspace_size,
     fwd,
     workspace_size,
 )
 
 __all__ = ["fwd", "bwd_preprocess", "bwd", "attention_backward", "bwd_main", "bwd_postprocess", "workspace_size",
-           "alloc_workspace", "check_device_error", "HostRunner", "decode", "decode_workspace_size"]
+           "alloc_workspace", "check_device_error", "HostRunner", "decode", "decode_workspace_size",
+           "decode_slices", "decode_merge", "alloc_decode_workspace", "DecodeHostRunner"]

@@ -35,6 +35,8 @@ _SIGS = {
     "fa_bwd_noalloc": ([_vp] * 10 + [_i] * 7 + [_vp], _i),
     "fa_decode_workspace_size": ([_i] * 6, ctypes.c_size_t),
     "fa_decode": ([_vp] * 6 + [ctypes.c_size_t] + [_i] * 8 + [_vp], _i),
+    "fa_decode_slices": ([_vp] * 4 + [ctypes.c_size_t] + [_i] * 8 + [_vp], _i),
+    "fa_decode_merge": ([_vp, ctypes.c_size_t, _vp, _vp] + [_i] * 7 + [_vp], _i),
     "fa_check_device_error": ([_vp], _i),
     "fa_last_error_site": ([], ctypes.c_uint),
     "fa_selftest_bounded_wait": ([ctypes.c_ulonglong, _vp], _i),

@@ -74,33 +74,73 @@ def decode_workspace_size(B: int, Lq: int, Lk: int, H: int, Hkv: int, D: int) ->
     return int(_lib.load().fa_decode_workspace_size(B, Lq, Lk, H, Hkv, D))
 
 
-def decode(q, k, v, causal: bool = False, out=None, lse=None, workspace=None, stream=None):
-    """Split-KV decoding: O, LSE = attention(Q, K, V) for few queries against
-    many keys.  q [B, Lq, H, D]; k, v [B, Lk, Hkv, D] with (H / Hkv) * Lq <= 128.
-    Same result and masking rule as ``fwd``.  ``workspace`` (a CUDA byte
-    tensor of at least ``decode_workspace_size`` bytes) is allocated when not
-    given."""
+def _decode_shapes(q, k, v):
     B, Lq, H, D = q.shape
     Lk, Hkv = k.shape[1], k.shape[2]
     _need(q, "q")
     _need(k, "k", (B, Lk, Hkv, D), q.dtype)
     _need(v, "v", (B, Lk, Hkv, D), q.dtype)
+    return B, Lq, Lk, H, Hkv, D
+
+
+def _decode_outputs(q, B, Lq, H, out, lse):
     if out is None:
         out = torch.empty_like(q)
     if lse is None:
         lse = torch.empty(B, H, Lq, device=q.device, dtype=torch.float32)
     _need(out, "out", q.shape, q.dtype)
     _need(lse, "lse", (B, H, Lq), torch.float32)
+    return out, lse
+
+
+def _nbytes(t) -> int:
+    _need(t, "workspace")
+    return t.numel() * t.element_size()
+
+
+def alloc_decode_workspace(B, Lq, Lk, H, Hkv, D, device) -> torch.Tensor:
+    """A byte tensor large enough for ``decode`` on ``device``."""
+    with torch.cuda.device(device):
+        n = decode_workspace_size(B, Lq, Lk, H, Hkv, D)
+    return torch.empty(max(n, 16), device=device, dtype=torch.uint8)
+
+
+def decode(q, k, v, causal: bool = False, out=None, lse=None, workspace=None, stream=None):
+    """Split-KV decoding: O, LSE = attention(Q, K, V) for few queries against
+    many keys.  q [B, Lq, H, D]; k, v [B, Lk, Hkv, D] with (H / Hkv) * Lq <= 128.
+    Same result and masking rule as ``fwd``.  ``workspace`` (a CUDA byte
+    tensor of at least ``decode_workspace_size`` bytes) is allocated when not
+    given."""
+    B, Lq, Lk, H, Hkv, D = _decode_shapes(q, k, v)
+    out, lse = _decode_outputs(q, B, Lq, H, out, lse)
     if workspace is None:
-        workspace = torch.empty(max(decode_workspace_size(B, Lq, Lk, H, Hkv, D), 16),
-                                device=q.device, dtype=torch.uint8)
-    _need(workspace, "workspace")
-    nbytes = workspace.numel() * workspace.element_size()
+        workspace = alloc_decode_workspace(B, Lq, Lk, H, Hkv, D, q.device)
     st = _lib.load().fa_decode(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
-                               lse.data_ptr(), workspace.data_ptr(), nbytes, B, Lq, Lk, H, Hkv, D,
-                               int(bool(causal)), _dtype_code(q), _stream(stream))
+                               lse.data_ptr(), workspace.data_ptr(), _nbytes(workspace), B, Lq, Lk,
+                               H, Hkv, D, int(bool(causal)), _dtype_code(q), _stream(stream))
     _lib.check("fa_decode", st)
     return out, lse
+
+
+def decode_slices(q, k, v, workspace, causal: bool = False, stream=None):
+    """First stage of ``decode``: per-slice partial O and LSE into ``workspace``."""
+    B, Lq, Lk, H, Hkv, D = _decode_shapes(q, k, v)
+    st = _lib.load().fa_decode_slices(q.data_ptr(), k.data_ptr(), v.data_ptr(),
+                                      workspace.data_ptr(), _nbytes(workspace), B, Lq, Lk, H, Hkv,
+                                      D, int(bool(causal)), _dtype_code(q), _stream(stream))
+    _lib.check("fa_decode_slices", st)
+
+
+def decode_merge(workspace, out, lse, Lk: int, Hkv: int, stream=None):
+    """Second stage of ``decode``: merge the slices into ``out`` [B, Lq, H, D]
+    and ``lse`` [B, H, Lq] for a key length Lk and Hkv K/V heads."""
+    B, Lq, H, D = out.shape
+    _need(out, "out")
+    _need(lse, "lse", (B, H, Lq), torch.float32)
+    st = _lib.load().fa_decode_merge(workspace.data_ptr(), _nbytes(workspace), out.data_ptr(),
+                                     lse.data_ptr(), B, Lq, Lk, H, Hkv, D, _dtype_code(out),
+                                     _stream(stream))
+    _lib.check("fa_decode_merge", st)
 
 
 def workspace_size(B: int, L: int, H: int, D: int) -> int:
@@ -271,4 +311,41 @@ class HostRunner:
         for name, src in (("o", self.o), ("lse", self.lse), ("dq", self.dq), ("dk", self.dk),
                           ("dv", self.dv)):
             self.h_out[name].copy_(src, non_blocking=True)
+        return self.h_out
+
+
+class DecodeHostRunner:
+    """Split-KV decoding for host-resident tensors through pinned buffers.
+
+    ``run(q, k, v)`` copies the CPU inputs to the device, runs ``decode`` and
+    copies O and LSE back into pinned host tensors (returned).  Device buffers
+    and the workspace are allocated once and reused.
+    """
+
+    def __init__(self, B, Lq, Lk, H, Hkv, D, dtype=torch.bfloat16, causal=False, device="cuda"):
+        self.causal = causal
+        dev = torch.device(device)
+        self.q = torch.empty(B, Lq, H, D, dtype=dtype, device=dev)
+        self.k = torch.empty(B, Lk, Hkv, D, dtype=dtype, device=dev)
+        self.v = torch.empty_like(self.k)
+        self.o = torch.empty_like(self.q)
+        self.lse = torch.empty(B, H, Lq, dtype=torch.float32, device=dev)
+        self.ws = alloc_decode_workspace(B, Lq, Lk, H, Hkv, D, dev)
+        pin = dict(pin_memory=True)
+        self.h_out = {"o": torch.empty(self.o.shape, dtype=dtype, **pin),
+                      "lse": torch.empty(self.lse.shape, dtype=torch.float32, **pin)}
+
+    def h2d_bytes(self) -> int:
+        return sum(t.numel() * t.element_size() for t in (self.q, self.k, self.v))
+
+    def d2h_bytes(self) -> int:
+        return sum(t.numel() * t.element_size() for t in self.h_out.values())
+
+    def run(self, q, k, v, stream=None):
+        for dst, src in ((self.q, q), (self.k, k), (self.v, v)):
+            dst.copy_(src, non_blocking=True)
+        decode(self.q, self.k, self.v, self.causal, out=self.o, lse=self.lse, workspace=self.ws,
+               stream=stream)
+        self.h_out["o"].copy_(self.o, non_blocking=True)
+        self.h_out["lse"].copy_(self.lse, non_blocking=True)
         return self.h_out

@@ -142,17 +142,44 @@ size_t fa_decode_workspace_size(int B, int Lq, int Lk, int H, int Hkv, int D) {
   return fa::decode_workspace_size(B, Lq, Lk, H, Hkv, D);
 }
 
-fa_status fa_decode(const void* Q, const void* K, const void* V, void* O, float* LSE,
-                    void* workspace, size_t workspace_bytes, int B, int Lq, int Lk, int H, int Hkv,
-                    int D, int causal, int dtype, void* stream) {
+namespace {
+fa_status check_decode(int B, int Lq, int Lk, int H, int Hkv, int D, int causal, int dtype) {
   fa_status st = check_shape(B, Lq, Lk, H, Hkv, D, dtype);
   if (st != FA_OK) return st;
   if (causal && Lk < Lq) return FA_ERR_INVALID_ARG;
   if (static_cast<long long>(H / Hkv) * Lq > 128) return FA_ERR_UNSUPPORTED;
+  return FA_OK;
+}
+}  // namespace
+
+fa_status fa_decode(const void* Q, const void* K, const void* V, void* O, float* LSE,
+                    void* workspace, size_t workspace_bytes, int B, int Lq, int Lk, int H, int Hkv,
+                    int D, int causal, int dtype, void* stream) {
+  const fa_status st = check_decode(B, Lq, Lk, H, Hkv, D, causal, dtype);
+  if (st != FA_OK) return st;
   if (!ptr_ok(Q) || !ptr_ok(K) || !ptr_ok(V) || !ptr_ok(O) || !ptr_ok(LSE) || !ptr_ok(workspace))
     return FA_ERR_INVALID_ARG;
   return fa::run_decode(Q, K, V, O, LSE, workspace, workspace_bytes, B, Lq, Lk, H, Hkv, D, causal,
                         dtype, static_cast<cudaStream_t>(stream));
+}
+
+fa_status fa_decode_slices(const void* Q, const void* K, const void* V, void* workspace,
+                           size_t workspace_bytes, int B, int Lq, int Lk, int H, int Hkv, int D,
+                           int causal, int dtype, void* stream) {
+  const fa_status st = check_decode(B, Lq, Lk, H, Hkv, D, causal, dtype);
+  if (st != FA_OK) return st;
+  if (!ptr_ok(Q) || !ptr_ok(K) || !ptr_ok(V) || !ptr_ok(workspace)) return FA_ERR_INVALID_ARG;
+  return fa::run_decode_slices(Q, K, V, workspace, workspace_bytes, B, Lq, Lk, H, Hkv, D, causal,
+                               dtype, static_cast<cudaStream_t>(stream));
+}
+
+fa_status fa_decode_merge(const void* workspace, size_t workspace_bytes, void* O, float* LSE, int B,
+                          int Lq, int Lk, int H, int Hkv, int D, int dtype, void* stream) {
+  const fa_status st = check_decode(B, Lq, Lk, H, Hkv, D, 0, dtype);
+  if (st != FA_OK) return st;
+  if (!ptr_ok(workspace) || !ptr_ok(O) || !ptr_ok(LSE)) return FA_ERR_INVALID_ARG;
+  return fa::run_decode_merge(workspace, workspace_bytes, O, LSE, B, Lq, Lk, H, Hkv, D, dtype,
+                              static_cast<cudaStream_t>(stream));
 }
 
 fa_status fa_check_device_error(void* stream) {

@@ -66,23 +66,34 @@ size_t decode_workspace_bytes(const DecodePlan& pl, int B, int Lq, int H, int D)
   return align256(rows * D * sizeof(float)) + align256(rows * sizeof(float));
 }
 
+namespace {
+
+struct WsView {
+  float* part_o;
+  float* part_lse;
+};
+
+WsView ws_view(void* ws, const DecodePlan& pl, int B, int Lq, int H, int D) {
+  const size_t rows_all = static_cast<size_t>(pl.nsplit) * B * H * Lq;
+  return {static_cast<float*>(ws),
+          reinterpret_cast<float*>(static_cast<char*>(ws) + align256(rows_all * D * sizeof(float)))};
+}
+
 template <int D, bool BF16>
-static fa_status launch_decode(const void* Q, const void* K, const void* V, void* O, float* LSE,
-                               void* ws, size_t ws_bytes, int B, int Lq, int Lk, int H, int Hkv,
-                               int causal, cudaStream_t s) {
+fa_status launch_slices(const void* Q, const void* K, const void* V, void* ws, size_t ws_bytes,
+                        int B, int Lq, int Lk, int H, int Hkv, int causal, cudaStream_t s) {
   using Ly = DecLayout<D>;
   const DecodePlan pl = decode_plan(B, Lq, Lk, H, Hkv, sm_count());
-  const size_t need = decode_workspace_bytes(pl, B, Lq, H, D);
-  if (ws_bytes < need) return FA_ERR_SCRATCH_TOO_SMALL;
+  if (ws_bytes < decode_workspace_bytes(pl, B, Lq, H, D)) return FA_ERR_SCRATCH_TOO_SMALL;
   const int g = H / Hkv;
   CUtensorMap tq, tk, tv;
   if (!make_group_map(&tq, Q, B, Lq, H, g, D, BF16) || !make_bshd_map(&tk, K, B, Lk, Hkv, D, BF16) ||
       !make_bshd_map(&tv, V, B, Lk, Hkv, D, BF16))
     return FA_ERR_CUDA;
+  const WsView w = ws_view(ws, pl, B, Lq, H, D);
   DecParams p;
-  const size_t rows_all = static_cast<size_t>(pl.nsplit) * B * H * Lq;
-  p.part_o = static_cast<float*>(ws);
-  p.part_lse = reinterpret_cast<float*>(static_cast<char*>(ws) + align256(rows_all * D * sizeof(float)));
+  p.part_o = w.part_o;
+  p.part_lse = w.part_lse;
   p.B = B;
   p.Lq = Lq;
   p.Lk = Lk;
@@ -102,23 +113,51 @@ static fa_status launch_decode(const void* Q, const void* K, const void* V, void
     return FA_ERR_CUDA;
   const long long grid = static_cast<long long>(B) * Hkv * pl.nsplit;
   kern<<<static_cast<unsigned>(grid), Ly::NTHREADS, Ly::SMEM_ALLOC, s>>>(tq, tk, tv, p);
-  if (cudaGetLastError() != cudaSuccess) return FA_ERR_CUDA;
+  return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+template <int D, bool BF16>
+fa_status launch_merge(const void* ws, size_t ws_bytes, void* O, float* LSE, int B, int Lq, int Lk,
+                       int H, int Hkv, cudaStream_t s) {
+  const DecodePlan pl = decode_plan(B, Lq, Lk, H, Hkv, sm_count());
+  if (ws_bytes < decode_workspace_bytes(pl, B, Lq, H, D)) return FA_ERR_SCRATCH_TOO_SMALL;
+  const WsView w = ws_view(const_cast<void*>(ws), pl, B, Lq, H, D);
   const int nrows = B * H * Lq;
-  fa_decode_combine_kernel<D, BF16><<<(nrows + 7) / 8, 256, 0, s>>>(p.part_o, p.part_lse, O, LSE, B,
+  fa_decode_combine_kernel<D, BF16><<<(nrows + 7) / 8, 256, 0, s>>>(w.part_o, w.part_lse, O, LSE, B,
                                                                     Lq, H, pl.nsplit);
   return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+}  // namespace
+
+fa_status run_decode_slices(const void* Q, const void* K, const void* V, void* ws, size_t ws_bytes,
+                            int B, int Lq, int Lk, int H, int Hkv, int D, int causal, int dtype,
+                            cudaStream_t s) {
+  const bool bf16 = dtype == FA_BF16;
+  if (D == 64)
+    return bf16 ? launch_slices<64, true>(Q, K, V, ws, ws_bytes, B, Lq, Lk, H, Hkv, causal, s)
+                : launch_slices<64, false>(Q, K, V, ws, ws_bytes, B, Lq, Lk, H, Hkv, causal, s);
+  return bf16 ? launch_slices<128, true>(Q, K, V, ws, ws_bytes, B, Lq, Lk, H, Hkv, causal, s)
+              : launch_slices<128, false>(Q, K, V, ws, ws_bytes, B, Lq, Lk, H, Hkv, causal, s);
+}
+
+fa_status run_decode_merge(const void* ws, size_t ws_bytes, void* O, float* LSE, int B, int Lq,
+                           int Lk, int H, int Hkv, int D, int dtype, cudaStream_t s) {
+  const bool bf16 = dtype == FA_BF16;
+  if (D == 64)
+    return bf16 ? launch_merge<64, true>(ws, ws_bytes, O, LSE, B, Lq, Lk, H, Hkv, s)
+                : launch_merge<64, false>(ws, ws_bytes, O, LSE, B, Lq, Lk, H, Hkv, s);
+  return bf16 ? launch_merge<128, true>(ws, ws_bytes, O, LSE, B, Lq, Lk, H, Hkv, s)
+              : launch_merge<128, false>(ws, ws_bytes, O, LSE, B, Lq, Lk, H, Hkv, s);
 }
 
 fa_status run_decode(const void* Q, const void* K, const void* V, void* O, float* LSE, void* ws,
                      size_t ws_bytes, int B, int Lq, int Lk, int H, int Hkv, int D, int causal,
                      int dtype, cudaStream_t s) {
-  const bool bf16 = dtype == FA_BF16;
-  if (D == 64) {
-    return bf16 ? launch_decode<64, true>(Q, K, V, O, LSE, ws, ws_bytes, B, Lq, Lk, H, Hkv, causal, s)
-                : launch_decode<64, false>(Q, K, V, O, LSE, ws, ws_bytes, B, Lq, Lk, H, Hkv, causal, s);
-  }
-  return bf16 ? launch_decode<128, true>(Q, K, V, O, LSE, ws, ws_bytes, B, Lq, Lk, H, Hkv, causal, s)
-              : launch_decode<128, false>(Q, K, V, O, LSE, ws, ws_bytes, B, Lq, Lk, H, Hkv, causal, s);
+  const fa_status st =
+      run_decode_slices(Q, K, V, ws, ws_bytes, B, Lq, Lk, H, Hkv, D, causal, dtype, s);
+  if (st != FA_OK) return st;
+  return run_decode_merge(ws, ws_bytes, O, LSE, B, Lq, Lk, H, Hkv, D, dtype, s);
 }
 
 size_t decode_workspace_size(int B, int Lq, int Lk, int H, int Hkv, int D) {

@@ -41,6 +41,11 @@ size_t decode_workspace_size(int B, int Lq, int Lk, int H, int Hkv, int D);
 fa_status run_decode(const void* Q, const void* K, const void* V, void* O, float* LSE, void* ws,
                      size_t ws_bytes, int B, int Lq, int Lk, int H, int Hkv, int D, int causal,
                      int dtype, cudaStream_t s);
+fa_status run_decode_slices(const void* Q, const void* K, const void* V, void* ws, size_t ws_bytes,
+                            int B, int Lq, int Lk, int H, int Hkv, int D, int causal, int dtype,
+                            cudaStream_t s);
+fa_status run_decode_merge(const void* ws, size_t ws_bytes, void* O, float* LSE, int B, int Lq,
+                           int Lk, int H, int Hkv, int D, int dtype, cudaStream_t s);
 unsigned int decode_read_error(cudaStream_t s);
 
 inline int padded_len(int L) { return (L + 127) / 128 * 128; }
