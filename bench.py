@@ -57,9 +57,18 @@ WORKLOADS = {
 }
 METRIC = "attention fwd/bwd TFLOP/s (fp16 B8 H32 L4096 D128) and % of GB300 TC peak"
 DECODE_METRIC = "attention split-KV decode GB/s (Q, K, V read + O, LSE written)"
-KERNEL_SOURCES = ["tiled_attention_fa_gb300/csrc/ptx.cuh", "tiled_attention_fa_gb300/csrc/common.cuh",
-                  "tiled_attention_fa_gb300/csrc/fwd.cuh", "tiled_attention_fa_gb300/csrc/bwd.cuh",
-                  "tiled_attention_fa_gb300/csrc/decode.cuh"]
+_CSRC = "tiled_attention_fa_gb300/csrc/"
+_COMMON = [_CSRC + "ptx.cuh", _CSRC + "common.cuh", _CSRC + "fwd.cuh"]
+# Sources each kernel is compiled from (a recorded DRAM figure is valid only
+# while these still hash to the value stored beside it).
+KERNEL_SOURCES = {
+    "fa_fwd_kernel": _COMMON,
+    "fa_bwd_prep_kernel": _COMMON + [_CSRC + "bwd.cuh"],
+    "fa_bwd_kernel": _COMMON + [_CSRC + "bwd.cuh"],
+    "fa_dq_convert_kernel": _COMMON + [_CSRC + "bwd.cuh"],
+    "fa_decode_kernel": _COMMON + [_CSRC + "decode.cuh"],
+    "fa_decode_combine_kernel": _COMMON + [_CSRC + "decode.cuh"],
+}
 
 
 def fwd_flops(B, H, L, D, causal, Lk=None):
@@ -93,9 +102,9 @@ def peaks():
         return 1900.0, 1700.0, 6800.0, "fallback"
 
 
-def source_hash():
+def source_hash(kernel):
     h = hashlib.sha256()
-    for p in KERNEL_SOURCES:
+    for p in KERNEL_SOURCES[kernel]:
         with open(os.path.join(ROOT, p), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
@@ -109,7 +118,7 @@ def recorded_traffic(kernel):
         with open(path) as fh:
             for line in fh:
                 f = dict(kv.split("=", 1) for kv in line.split() if "=" in kv)
-                if f.get("kernel") == kernel and f.get("src") == source_hash():
+                if f.get("kernel") == kernel and f.get("src") == source_hash(kernel):
                     return float(f["dram_bytes_per_launch"])
     except OSError:
         pass

@@ -526,3 +526,21 @@ def test_top_left_alignment_is_caught():
     o_full, _ = orc.forward(q, k, v, True)
     wrong = top_left(q[0, L - Lq:, 0], k[0, :, 0], v[0, :, 0])
     assert not np.allclose(wrong, o_full[0, L - Lq:, 0], atol=1e-6)
+
+
+def test_key_slices_merged_by_lse_equal_the_whole():
+    # Split-KV decoding rests on this identity: attention over disjoint key
+    # slices, merged with weights exp(LSE_s - LSE) where LSE = ln sum_s exp(LSE_s),
+    # is attention over all keys (checked on the oracle's own forward).
+    rng = np.random.default_rng(95)
+    Lq, Lk, D = 3, 50, 8
+    q, k, v = rng.standard_normal((Lq, D)), rng.standard_normal((Lk, D)), rng.standard_normal((Lk, D))
+    o_all, l_all = orc.unit_forward(q, k, v, False)
+    cuts = [0, 7, 8, 31, 50]
+    parts = [orc.unit_forward(q, k[a:b], v[a:b], False) for a, b in zip(cuts[:-1], cuts[1:])]
+    lses = np.stack([p[1] for p in parts])            # [slices, Lq]
+    lse = np.log(np.exp(lses).sum(axis=0))
+    w = np.exp(lses - lse)                            # [slices, Lq]
+    o = sum(w[s][:, None] * parts[s][0] for s in range(len(parts)))
+    np.testing.assert_allclose(lse, l_all, atol=1e-13)
+    np.testing.assert_allclose(o, o_all, atol=1e-13)
