@@ -55,6 +55,19 @@ softmax, no fusion):
   with dK and dV of a KV head summed over the query heads of its group (what
   differentiating through the head repeat gives).
 
+* FP8 forward (page "TileLang性能分析报告：H100上FlashAttention吞吐量达1.2PFlops",
+  section 生产环境部署建议, item 1, which names FP8 mixed precision and an FP8
+  example and gives nothing more): reading taken here is attention over
+  inputs given as 8-bit E4M3 codes with one fp32 scale per tensor, i.e. the
+  forward above applied to decode(Q8) * q_scale, decode(K8) * k_scale,
+  decode(V8) * v_scale.  decode follows the E4M3 format of the OCP 8-bit
+  floating point specification (the variant without infinities): sign in
+  bit 7, a 4-bit exponent with bias 7 in bits 6-3, a 3-bit mantissa in bits
+  2-0; exponent 0 holds the subnormals m/8 * 2^-6; exponent 15 with mantissa
+  7 is NaN.  The result is the exact attention of the dequantised inputs;
+  a kernel that rounds P to E4M3 before the PV product differs from it by
+  that rounding, for which the tests carry an error bound.
+
 All arithmetic is numpy float64; matmul and exp are library primitives.  For
 very long sequences the per-unit functions may process query rows in panels:
 each row's softmax still sees all of its keys, so the result is the same
@@ -74,6 +87,8 @@ __all__ = [
     "backward",
     "bwd_preprocess",
     "storage_round",
+    "e4m3_decode",
+    "forward_fp8",
 ]
 
 
@@ -250,3 +265,25 @@ def backward(q, k, v, do, causal: bool, o_round=None):
             dv[b, :, hk, :] += gv
             delta[b, h, :] = dl
     return dq, dk, dv, delta
+
+
+def e4m3_decode(codes) -> np.ndarray:
+    """float64 value of each E4M3 code (uint8 array): (-1)^s * 2^(e-7) * (1 + m/8)
+    for exponent field e in 1..15, (-1)^s * 2^-6 * m/8 for e = 0, NaN for the
+    all-ones exponent and mantissa."""
+    c = np.asarray(codes, dtype=np.uint8).astype(np.int64)
+    sign = np.where(c & 0x80, -1.0, 1.0)
+    e = (c >> 3) & 0xF
+    m = (c & 0x7).astype(np.float64)
+    normal = sign * np.ldexp(1.0 + m / 8.0, (e - 7).astype(np.int64))
+    subnormal = sign * np.ldexp(m / 8.0, -6)
+    val = np.where(e == 0, subnormal, normal)
+    return np.where((e == 15) & ((c & 0x7) == 7), np.nan, val)
+
+
+def forward_fp8(q8, k8, v8, q_scale: float, k_scale: float, v_scale: float, causal: bool):
+    """Forward on per-tensor-scaled E4M3 inputs: ``forward`` of the decoded
+    values times their scales.  q8 [B, Lq, H, D], k8, v8 [B, Lk, Hkv, D] as
+    uint8 codes.  Returns O [B, Lq, H, D], LSE [B, H, Lq] (float64)."""
+    return forward(e4m3_decode(q8) * float(q_scale), e4m3_decode(k8) * float(k_scale),
+                   e4m3_decode(v8) * float(v_scale), causal)

@@ -544,3 +544,94 @@ def test_key_slices_merged_by_lse_equal_the_whole():
     o = sum(w[s][:, None] * parts[s][0] for s in range(len(parts)))
     np.testing.assert_allclose(lse, l_all, atol=1e-13)
     np.testing.assert_allclose(o, o_all, atol=1e-13)
+
+
+# ---------------------------------------------------------------- FP8 (E4M3) inputs
+
+E4M3_HAND = {0x00: 0.0, 0x01: 2.0 ** -9, 0x07: 7 * 2.0 ** -9, 0x08: 2.0 ** -6, 0x0F: 1.875 * 2.0 ** -6,
+             0x38: 1.0, 0x3C: 1.5, 0x40: 2.0, 0x7E: 448.0, 0x80: -0.0, 0xB8: -1.0, 0xFE: -448.0}
+
+
+def test_e4m3_decode_matches_torch_on_every_code():
+    codes = np.arange(256, dtype=np.uint8)
+    mine = orc.e4m3_decode(codes)
+    ref = torch.from_numpy(codes).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    assert np.array_equal(np.isnan(mine), np.isnan(ref))
+    assert np.isnan(mine).sum() == 2                       # 0x7F and 0xFF only
+    ok = ~np.isnan(ref)
+    assert np.array_equal(mine[ok], ref[ok])
+
+
+def test_e4m3_decode_hand_values():
+    for code, val in E4M3_HAND.items():
+        got = orc.e4m3_decode(np.array([code], dtype=np.uint8))[0]
+        assert got == val and math.copysign(1.0, got) == math.copysign(1.0, val), hex(code)
+
+
+def _fp8_case(seed, B=1, Lq=9, Lk=23, H=4, Hkv=2, D=16):
+    """Random E4M3 codes with exponent field <= 8 (|x| < 4, no NaN)."""
+    rng = np.random.default_rng(seed)
+
+    def codes(shape):
+        sign = rng.integers(0, 2, shape) << 7
+        exp = rng.integers(0, 9, shape) << 3
+        man = rng.integers(0, 8, shape)
+        return (sign | exp | man).astype(np.uint8)
+    return codes((B, Lq, H, D)), codes((B, Lk, Hkv, D)), codes((B, Lk, Hkv, D))
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_fp8_forward_is_forward_of_dequantised_inputs(causal):
+    q8, k8, v8 = _fp8_case(101)
+    o, lse = orc.forward_fp8(q8, k8, v8, 0.5, 0.25, 3.0, causal)
+    assert not np.isnan(o).any()
+    v_scaled_o, _ = orc.forward_fp8(q8, k8, v8, 0.5, 0.25, 6.0, causal)
+    np.testing.assert_allclose(v_scaled_o, 2.0 * o, rtol=1e-14, atol=0)          # V scale is linear
+    o2, lse2 = orc.forward_fp8(q8, k8, v8, 0.25, 0.5, 3.0, causal)
+    np.testing.assert_allclose(o2, o, atol=1e-13)                                # only qs*ks matters
+    np.testing.assert_allclose(lse2, lse, atol=1e-13)
+    o3, lse3 = orc.forward_fp8(q8, k8, v8, 1.0, 0.25, 3.0, causal)               # doubles every score
+    qd = orc.e4m3_decode(q8)
+    ref3, ref_l3 = orc.forward(qd, orc.e4m3_decode(k8) * 0.25, orc.e4m3_decode(v8) * 3.0, causal)
+    np.testing.assert_allclose(o3, ref3, atol=1e-13)
+    np.testing.assert_allclose(lse3, ref_l3, atol=1e-13)
+
+
+def test_planted_e4m3_mistakes_are_caught():
+    codes = np.arange(256, dtype=np.uint8)
+    torch_ref = torch.from_numpy(codes).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+
+    def bias8(c):          # exponent bias 8 instead of 7
+        return orc.e4m3_decode(c) / 2.0
+
+    def implicit_one(c):   # subnormals decoded with the implicit leading 1
+        c = np.asarray(c)
+        e = (c >> 3) & 0xF
+        v = orc.e4m3_decode(c)
+        return np.where(e == 0, np.sign(v + 0.0) * np.ldexp(1.0 + (c & 7) / 8.0, -6), v)
+
+    def no_sign(c):
+        return np.abs(orc.e4m3_decode(c))
+
+    def mant16(c):         # mantissa read as sixteenths
+        c = np.asarray(c)
+        e = ((c >> 3) & 0xF).astype(np.int64)
+        return np.where(e == 0, orc.e4m3_decode(c), np.ldexp(1.0 + (c & 7) / 16.0, e - 7))
+
+    for bad in (bias8, implicit_one, no_sign, mant16):
+        vals = bad(codes)
+        ok = ~np.isnan(torch_ref)
+        hand_fail = any(bad(np.array([k], dtype=np.uint8))[0] != v for k, v in E4M3_HAND.items())
+        torch_fail = not np.array_equal(vals[ok], torch_ref[ok])
+        assert hand_fail and torch_fail, bad.__name__
+
+
+def test_fp8_inputs_are_seeded_codes_with_amax_scales():
+    from tiled_attention_fa_gb300.inputs import make_qkv_fp8
+    a = make_qkv_fp8(1, 3, 40, 4, 2, 16, seed=5)
+    b = make_qkv_fp8(1, 3, 40, 4, 2, 16, seed=5)
+    for x, y in zip(a, b):
+        assert (x == y).all() if isinstance(x, torch.Tensor) else x == y
+    for codes, s in zip(a[:3], a[3:]):
+        vals = orc.e4m3_decode(codes.numpy())
+        assert not np.isnan(vals).any() and np.abs(vals).max() == 448.0 and s > 0

@@ -58,6 +58,27 @@ def make_qkv_kv(B: int, Lq: int, Lk: int, H: int, Hkv: int, D: int, dtype="fp16"
     return q, k, v, do
 
 
+def make_qkv_fp8(B: int, Lq: int, Lk: int, H: int, Hkv: int, D: int, seed: int = 0):
+    """E4M3 inputs with one fp32 scale per tensor: (q8, k8, v8, q_scale, k_scale,
+    v_scale), the codes as uint8 CPU tensors.  Q, K, V are drawn as in
+    ``make_qkv_kv``; each tensor's scale is its largest magnitude over 448 (the
+    largest E4M3 value) and its codes are torch's round-to-nearest cast of
+    x / scale to float8_e4m3fn."""
+    g = torch.Generator(device="cpu")
+    g.manual_seed(int(seed))
+    q = torch.randn(B, Lq, H, D, generator=g, dtype=torch.float32)
+    k = torch.randn(B, Lk, Hkv, D, generator=g, dtype=torch.float32)
+    v = torch.randn(B, Lk, Hkv, D, generator=g, dtype=torch.float32)
+    out = []
+    scales = []
+    for x in (q, k, v):
+        s = float(x.abs().max()) / 448.0 if x.numel() else 1.0
+        s = s if s > 0 else 1.0
+        out.append((x / s).to(torch.float8_e4m3fn).view(torch.uint8))
+        scales.append(s)
+    return out[0], out[1], out[2], scales[0], scales[1], scales[2]
+
+
 def make_unit(L: int, D: int, dtype="fp16", seed: int = 0, group: int = 1):
     """One (batch, kv-head) unit with ``group`` query heads: shapes [1, L, group, D]
     for Q/dO and [1, L, 1, D] for K/V.  Used for small, fast cases."""
