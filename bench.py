@@ -54,9 +54,14 @@ WORKLOADS = {
                                                       Hkv=8, D=128, dtype="bf16"),
     "decode_b8_h32_hkv8_lq4_lk32768_d128_bf16": dict(mode="decode", B=8, L=4, Lk=32768, H=32,
                                                      Hkv=8, D=128, dtype="bf16"),
+    # forward on E4M3 inputs (per-tensor scales), bf16 output
+    "fp8_b8_h32_l4096_d128": dict(mode="fp8", B=8, L=4096, H=32, Hkv=32, D=128, dtype="bf16"),
+    "fp8_gqa_b4_h32_hkv8_l4096_d128": dict(mode="fp8", B=4, L=4096, H=32, Hkv=8, D=128,
+                                           dtype="bf16"),
 }
 METRIC = "attention fwd/bwd TFLOP/s (fp16 B8 H32 L4096 D128) and % of GB300 TC peak"
 DECODE_METRIC = "attention split-KV decode GB/s (Q, K, V read + O, LSE written)"
+FP8_METRIC = "attention forward on E4M3 inputs TFLOP/s (4*B*H*L^2*D, halved causal)"
 _CSRC = "tiled_attention_fa_gb300/csrc/"
 _COMMON = [_CSRC + "ptx.cuh", _CSRC + "common.cuh", _CSRC + "fwd.cuh"]
 # Sources each kernel is compiled from (a recorded DRAM figure is valid only
@@ -68,6 +73,7 @@ KERNEL_SOURCES = {
     "fa_dq_convert_kernel": _COMMON + [_CSRC + "bwd.cuh"],
     "fa_decode_kernel": _COMMON + [_CSRC + "decode.cuh"],
     "fa_decode_combine_kernel": _COMMON + [_CSRC + "decode.cuh"],
+    "fa_fwd_kernel_e4m3": _COMMON,
 }
 
 
@@ -91,6 +97,10 @@ def decode_bytes(B, Lq, Lk, H, Hkv, D, esize=2):
 
 def is_decode():
     return WORK.get("mode") == "decode"
+
+
+def is_fp8():
+    return WORK.get("mode") == "fp8"
 
 
 def peaks():
@@ -244,6 +254,8 @@ def reference_arm(args):
         return 0
     if is_decode():
         return decode_reference_arm(args, world)
+    if is_fp8():
+        return fp8_reference_arm(args, world)
     L, D = WORK["L"], WORK["D"]
     qs, ks, vs, dos = cpu_unit_inputs()
     flops_unit = step_flops(1, 1, L, D, args.causal)
@@ -282,6 +294,8 @@ def config_dict(args, world):
 def ours_arm(args):
     if is_decode():
         return decode_arm(args)
+    if is_fp8():
+        return fp8_arm(args)
     import torch
     import tiled_attention_fa_gb300 as fa
     from tiled_attention_fa_gb300 import _lib, replicas
@@ -619,6 +633,169 @@ def decode_arm(args):
             "dtype": WORK["dtype"], "data": "synthetic", "config": decode_config(args, world),
             "tflops": tflops, "kernels": kernels, "roofline": roof, "clocks": clocks, "e2e": e2e,
             "cpu_baseline": cpu, "gpu_launches": 2 * args.steps,
+        }
+        print(json.dumps(out), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+# --------------------------------------------------------------------- E4M3 forward
+
+def fp8_config(args, world):
+    B, L, H, Hkv, D = (WORK[x] for x in ("B", "L", "H", "Hkv", "D"))
+    return {"workload": f"attention forward E4M3 inputs B{B} H{H} Hkv{Hkv} L{L} D{D} -> "
+                        f"{WORK['dtype']} {'causal' if args.causal else 'non-causal'}",
+            "B": B, "L": L, "H": H, "Hkv": Hkv, "D": D, "causal": bool(args.causal),
+            "per_gpu_batch": B, "global_batch": B * world, "parallelism": f"replicas x{world}",
+            "l2": (f"inputs larger than L2 (Q {B * L * H * D // 10**6} MB, K and V "
+                   f"{2 * B * L * Hkv * D // 10**6} MB)")}
+
+
+def time_oracle_fp8_units(q8, k8, v8, scales, causal, n_units, budget_s):
+    """Oracle FP8 forward of one (b, h) unit at a time (decode + forward)."""
+    from oracle import fa_oracle as orc
+    qs, ks, vs = scales
+    H, Hkv = q8.shape[2], k8.shape[2]
+    done, t0 = 0, time.perf_counter()
+    for u in range(n_units):
+        h = u % H
+        hk = orc.kv_head(h, H, Hkv)
+        orc.unit_forward(orc.e4m3_decode(q8[0, :, h]) * qs, orc.e4m3_decode(k8[0, :, hk]) * ks,
+                         orc.e4m3_decode(v8[0, :, hk]) * vs, causal)
+        done += 1
+        if time.perf_counter() - t0 > budget_s:
+            break
+    return done, time.perf_counter() - t0
+
+
+def fp8_unit_inputs(seed=0):
+    from tiled_attention_fa_gb300.inputs import make_qkv_fp8
+    q8, k8, v8, qs, ks, vs = make_qkv_fp8(1, WORK["L"], WORK["L"], WORK["H"], WORK["Hkv"],
+                                          WORK["D"], seed=seed)
+    return q8.numpy(), k8.numpy(), v8.numpy(), (qs, ks, vs)
+
+
+def fp8_reference_arm(args, world):
+    L, D = WORK["L"], WORK["D"]
+    q8, k8, v8, sc = fp8_unit_inputs()
+    time_oracle_fp8_units(q8, k8, v8, sc, args.causal, args.warmup, 1e9)
+    n, secs = time_oracle_fp8_units(q8, k8, v8, sc, args.causal, args.steps, 1e9)
+    value = n * fwd_flops(1, 1, L, D, args.causal) / secs / 1e12
+    sample = (f"oracle fp64 forward of one (batch, head) unit of E4M3 inputs per step (L={L}, "
+              f"D={D}, {'causal' if args.causal else 'non-causal'}), {n} steps")
+    out = {
+        "impl": "reference", "metric": FP8_METRIC, "value": value, "unit": "TFLOP/s",
+        "n_gpus": world, "steps": n, "warmup": args.warmup, "ms_per_step": secs / n * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": fp8_config(args, world),
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": blas_threads(),
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(out), flush=True)
+    return 0
+
+
+def fp8_arm(args):
+    import torch
+    import tiled_attention_fa_gb300 as fa
+    from tiled_attention_fa_gb300 import _lib, replicas
+
+    world, rank, local = dist_setup()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    replicas.init("nccl", dev)
+    _lib.load()  # fails loudly without the built library
+
+    B, L, H, Hkv, D = (WORK[x] for x in ("B", "L", "H", "Hkv", "D"))
+    causal = bool(args.causal)
+    out_dt = torch.bfloat16 if WORK["dtype"] == "bf16" else torch.float16
+    g = torch.Generator(device=dev).manual_seed(replicas.replica_seed(777, rank))
+
+    def codes(*shape):
+        x = torch.randn(*shape, device=dev, dtype=torch.float32, generator=g)
+        s = float(x.abs().max()) / 448.0
+        return (x / s).to(torch.float8_e4m3fn).view(torch.uint8), s
+
+    (q8, qs), (k8, ks), (v8, vs) = codes(B, L, H, D), codes(B, L, Hkv, D), codes(B, L, Hkv, D)
+    o = torch.empty(B, L, H, D, device=dev, dtype=out_dt)
+    lse = torch.empty(B, H, L, device=dev, dtype=torch.float32)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        fa.fwd_fp8(q8, k8, v8, qs, ks, vs, causal, out_dtype=out_dt, out=o, lse=lse, stream=stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    fa.check_device_error()
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    sampler = ClockSampler(local, enabled=not args.no_clocks)
+    replicas.barrier()
+    torch.cuda.synchronize()
+    sampler.start()
+    t_start.record(stream)
+    for _ in range(args.steps):
+        step()
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    replicas.barrier()
+    clocks = sampler.stop()
+    fa.check_device_error()
+    ms = t_start.elapsed_time(t_end) / args.steps          # one launch per step
+    ms_per_step = replicas.max_over_ranks(ms, dev)
+    flops = fwd_flops(B, H, L, D, causal)
+    ach = flops / (ms * 1e-3) / 1e12
+    burst, sustained, hbm, src = peaks()
+    # E4M3 dense tensor rate = 2x the 16-bit rate on this part (4.5 vs 2.25 PFLOP/s nominal).
+    peak = 2.0 * sustained
+    roof = {"kernel": "fa_fwd_kernel (E4M3)", "bound": "tensor", "achieved": ach, "peak": peak,
+            "unit": "TFLOP/s", "frac": ach / peak,
+            "peak_source": f"{src} bf16 sustained x 2 (nominal E4M3 / BF16 dense ratio)",
+            "frac_of_burst": ach / (2.0 * burst), "frac_of_16bit_sustained": ach / sustained,
+            "traffic": recorded_traffic("fa_fwd_kernel_e4m3")}
+    value = replicas.aggregate_rate(flops, world, ms_per_step * 1e-3) / 1e12
+
+    e2e = None
+    if not args.no_e2e:
+        runner = fa.Fp8HostRunner(B, L, L, H, Hkv, D, out_dt, causal, dev)
+        hq, hk, hv = (x.cpu().pin_memory() for x in (q8, k8, v8))
+        runner.run(hq, hk, hv, qs, ks, vs)
+        torch.cuda.synchronize()
+        n_e2e = max(3, min(args.steps, 10))
+        s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        replicas.barrier()
+        torch.cuda.synchronize()
+        s0.record(stream)
+        for _ in range(n_e2e):
+            runner.run(hq, hk, hv, qs, ks, vs, stream=stream)
+        s1.record(stream)
+        torch.cuda.synchronize()
+        ems = replicas.max_over_ranks(s0.elapsed_time(s1) / n_e2e, dev)
+        e2e = {"value": replicas.aggregate_rate(flops, world, ems * 1e-3) / 1e12, "unit": "TFLOP/s",
+               "h2d_bytes_per_step": runner.h2d_bytes(), "d2h_bytes_per_step": runner.d2h_bytes(),
+               "ms_per_step": ems, "steps": n_e2e}
+        del runner
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        uq, uk, uv, sc = fp8_unit_inputs()
+        n, secs = time_oracle_fp8_units(uq, uk, uv, sc, causal, 100000, args.cpu_budget)
+        cpu = {"value": n * fwd_flops(1, 1, L, D, causal) / secs / 1e12, "unit": "TFLOP/s",
+               "cores": blas_threads(), "kind": "oracle",
+               "sample": f"{n} (batch, head) unit(s) of the workload, E4M3 decode + forward in "
+                         f"fp64 ({secs:.1f} s)"}
+
+    if rank == 0:
+        out = {
+            "metric": FP8_METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "e4m3",
+            "data": "synthetic", "config": fp8_config(args, world),
+            "kernels": {"fa_fwd_kernel (E4M3)": {"ms": ms, "tflops": ach}}, "roofline": roof,
+            "clocks": clocks, "e2e": e2e, "cpu_baseline": cpu, "gpu_launches": args.steps,
         }
         print(json.dumps(out), flush=True)
     if world > 1:

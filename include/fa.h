@@ -70,6 +70,27 @@ fa_status fa_fwd_kv(const void* Q, const void* K, const void* V, void* O, float*
                     int Lk, int H, int Hkv, int D, int causal, int dtype, void* stream);
 
 /*
+ * Forward on 8-bit inputs: Q8, K8, V8 hold E4M3 codes (one byte per element,
+ * the OCP 8-bit floating point E4M3 format without infinities), in the
+ * layouts above, each with one fp32 scale: the call computes the fa_fwd_kv
+ * result (same masking rule, past_len = Lk - Lq) for the dequantised inputs
+ *   Q = decode(Q8) * q_scale,  K = decode(K8) * k_scale,  V = decode(V8) * v_scale,
+ * writing O [B, Lq, H, D] in `out_dtype` (FA_F16 or FA_BF16) and LSE
+ * [B, H, Lq] in fp32.  Page "TileLang性能分析报告：H100上FlashAttention吞吐量达
+ * 1.2PFlops", section 生产环境部署建议, item 1 (FP8 mixed-precision compute);
+ * the loop is the online softmax of page "使用 TileLang 在 AMD GPU 上快速开发
+ * 高性能 Flash Attention", section K/V Tile 遍历与核心计算, with P rounded to
+ * E4M3 before the PV product, as that page rounds P to the input type.
+ * Scores accumulate in fp32 from exact products; the rounding of P is the
+ * one approximation (relative error at most 2^-4 per probability, absolute
+ * 2^-10 below 2^-6).  Requires D = 128 (FA_ERR_UNSUPPORTED otherwise) and
+ * finite scales > 0 (FA_ERR_INVALID_ARG otherwise).
+ */
+fa_status fa_fwd_fp8(const void* Q8, const void* K8, const void* V8, float q_scale,
+                     float k_scale, float v_scale, void* O, float* LSE, int B, int Lq, int Lk,
+                     int H, int Hkv, int D, int causal, int out_dtype, void* stream);
+
+/*
  * Split-KV decoding: the forward of fa_fwd_kv (same result, layouts, masking
  * rule and causal past_len = Lk - Lq) computed for few queries against many
  * keys.  The keys of each (batch, K/V head) are cut into equal slices of

@@ -8,6 +8,7 @@ package only marshals torch tensors into it.  Build the library with
 
 from .api import (  # noqa: F401
     DecodeHostRunner,
+    Fp8HostRunner,
     HostRunner,
     alloc_workspace,
     attention_backward,
@@ -22,9 +23,10 @@ from .api import (  # noqa: F401
     decode_slices,
     decode_workspace_size,
     fwd,
+    fwd_fp8,
     workspace_size,
 )
 
 __all__ = ["fwd", "bwd_preprocess", "bwd", "attention_backward", "bwd_main", "bwd_postprocess", "workspace_size",
            "alloc_workspace", "check_device_error", "HostRunner", "decode", "decode_workspace_size",
-           "decode_slices", "decode_merge", "alloc_decode_workspace", "DecodeHostRunner"]
+           "decode_slices", "decode_merge", "alloc_decode_workspace", "DecodeHostRunner", "fwd_fp8", "Fp8HostRunner"]

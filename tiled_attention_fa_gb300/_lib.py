@@ -26,6 +26,7 @@ _i = ctypes.c_int
 _SIGS = {
     "fa_fwd": ([_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, _vp], _i),
     "fa_fwd_kv": ([_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, _i, _vp], _i),
+    "fa_fwd_fp8": ([_vp] * 3 + [ctypes.c_float] * 3 + [_vp, _vp] + [_i] * 8 + [_vp], _i),
     "fa_bwd_preprocess": ([_vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _vp], _i),
     "fa_bwd_kv": ([_vp] * 11 + [_i] * 9 + [_vp], _i),
     "fa_bwd_workspace_size": ([_i, _i, _i, _i], ctypes.c_size_t),

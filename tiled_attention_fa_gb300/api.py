@@ -74,6 +74,41 @@ def decode_workspace_size(B: int, Lq: int, Lk: int, H: int, Hkv: int, D: int) ->
     return int(_lib.load().fa_decode_workspace_size(B, Lq, Lk, H, Hkv, D))
 
 
+_OUT = {torch.float16: _lib.FA_F16, torch.bfloat16: _lib.FA_BF16}
+
+
+def _codes(t: torch.Tensor, name: str, shape=None):
+    """E4M3 codes: a uint8 or float8_e4m3fn CUDA tensor."""
+    if t.dtype not in (torch.uint8, torch.float8_e4m3fn):
+        raise TypeError(f"{name} must hold E4M3 codes (uint8 or float8_e4m3fn), got {t.dtype}")
+    _need(t, name, shape)
+
+
+def fwd_fp8(q8, k8, v8, q_scale: float, k_scale: float, v_scale: float, causal: bool = False,
+            out_dtype=torch.bfloat16, out=None, lse=None, stream=None):
+    """O, LSE = attention of E4M3 inputs with per-tensor scales: the forward of
+    decode(q8) * q_scale, decode(k8) * k_scale, decode(v8) * v_scale.
+    q8 [B, Lq, H, 128]; k8, v8 [B, Lk, Hkv, 128]; O in ``out_dtype``."""
+    B, L, H, D = q8.shape
+    Lk, Hkv = k8.shape[1], k8.shape[2]
+    _codes(q8, "q8")
+    _codes(k8, "k8", (B, Lk, Hkv, D))
+    _codes(v8, "v8", (B, Lk, Hkv, D))
+    if out_dtype not in _OUT:
+        raise TypeError("out_dtype must be torch.float16 or torch.bfloat16")
+    if out is None:
+        out = torch.empty(B, L, H, D, device=q8.device, dtype=out_dtype)
+    if lse is None:
+        lse = torch.empty(B, H, L, device=q8.device, dtype=torch.float32)
+    _need(out, "out", (B, L, H, D), out_dtype)
+    _need(lse, "lse", (B, H, L), torch.float32)
+    st = _lib.load().fa_fwd_fp8(q8.data_ptr(), k8.data_ptr(), v8.data_ptr(), float(q_scale),
+                                float(k_scale), float(v_scale), out.data_ptr(), lse.data_ptr(), B, L,
+                                Lk, H, Hkv, D, int(bool(causal)), _OUT[out_dtype], _stream(stream))
+    _lib.check("fa_fwd_fp8", st)
+    return out, lse
+
+
 def _decode_shapes(q, k, v):
     B, Lq, H, D = q.shape
     Lk, Hkv = k.shape[1], k.shape[2]
@@ -346,6 +381,40 @@ class DecodeHostRunner:
             dst.copy_(src, non_blocking=True)
         decode(self.q, self.k, self.v, self.causal, out=self.o, lse=self.lse, workspace=self.ws,
                stream=stream)
+        self.h_out["o"].copy_(self.o, non_blocking=True)
+        self.h_out["lse"].copy_(self.lse, non_blocking=True)
+        return self.h_out
+
+
+class Fp8HostRunner:
+    """FP8 forward for host-resident E4M3 codes through pinned buffers:
+    ``run(q8, k8, v8, q_scale, k_scale, v_scale)`` copies the codes in, runs
+    ``fwd_fp8`` and copies O and LSE back into pinned host tensors."""
+
+    def __init__(self, B, Lq, Lk, H, Hkv, D=128, out_dtype=torch.bfloat16, causal=False,
+                 device="cuda"):
+        self.causal = causal
+        dev = torch.device(device)
+        self.q8 = torch.empty(B, Lq, H, D, dtype=torch.uint8, device=dev)
+        self.k8 = torch.empty(B, Lk, Hkv, D, dtype=torch.uint8, device=dev)
+        self.v8 = torch.empty_like(self.k8)
+        self.o = torch.empty(B, Lq, H, D, dtype=out_dtype, device=dev)
+        self.lse = torch.empty(B, H, Lq, dtype=torch.float32, device=dev)
+        pin = dict(pin_memory=True)
+        self.h_out = {"o": torch.empty(self.o.shape, dtype=out_dtype, **pin),
+                      "lse": torch.empty(self.lse.shape, dtype=torch.float32, **pin)}
+
+    def h2d_bytes(self) -> int:
+        return sum(t.numel() for t in (self.q8, self.k8, self.v8))
+
+    def d2h_bytes(self) -> int:
+        return sum(t.numel() * t.element_size() for t in self.h_out.values())
+
+    def run(self, q8, k8, v8, q_scale, k_scale, v_scale, stream=None):
+        for dst, src in ((self.q8, q8), (self.k8, k8), (self.v8, v8)):
+            dst.copy_(src, non_blocking=True)
+        fwd_fp8(self.q8, self.k8, self.v8, q_scale, k_scale, v_scale, self.causal,
+                out_dtype=self.o.dtype, out=self.o, lse=self.lse, stream=stream)
         self.h_out["o"].copy_(self.o, non_blocking=True)
         self.h_out["lse"].copy_(self.lse, non_blocking=True)
         return self.h_out

@@ -1,4 +1,5 @@
 // C ABI: argument validation and dispatch to the kernel units.
+#include <cmath>
 #include <cstdint>
 
 #include "../../include/fa.h"
@@ -55,6 +56,21 @@ fa_status fa_fwd_kv(const void* Q, const void* K, const void* V, void* O, float*
     return FA_ERR_INVALID_ARG;
   return fa::run_fwd(Q, K, V, O, LSE, B, Lq, Lk, H, Hkv, D, causal, dtype,
                      static_cast<cudaStream_t>(stream));
+}
+
+fa_status fa_fwd_fp8(const void* Q8, const void* K8, const void* V8, float q_scale,
+                     float k_scale, float v_scale, void* O, float* LSE, int B, int Lq, int Lk,
+                     int H, int Hkv, int D, int causal, int out_dtype, void* stream) {
+  fa_status st = check_shape(B, Lq, Lk, H, Hkv, D, out_dtype);
+  if (st != FA_OK) return st;
+  if (D != 128) return FA_ERR_UNSUPPORTED;
+  if (causal && Lk < Lq) return FA_ERR_INVALID_ARG;
+  for (float sc : {q_scale, k_scale, v_scale})
+    if (!(sc > 0.f) || !std::isfinite(sc)) return FA_ERR_INVALID_ARG;
+  if (!ptr_ok(Q8) || !ptr_ok(K8) || !ptr_ok(V8) || !ptr_ok(O) || !ptr_ok(LSE))
+    return FA_ERR_INVALID_ARG;
+  return fa::run_fwd_fp8(Q8, K8, V8, q_scale, k_scale, v_scale, O, LSE, B, Lq, Lk, H, Hkv, causal,
+                         out_dtype, static_cast<cudaStream_t>(stream));
 }
 
 fa_status fa_bwd_preprocess(const void* O, const void* dO, float* Delta, float* dq_accum, int B,

@@ -71,6 +71,22 @@ inline bool make_bshd_map(CUtensorMap* map, const void* ptr, int B, int L, int h
   return r == CUDA_SUCCESS;
 }
 
+// Same view for 8-bit E4M3 codes: dims {D, heads, L, B}, box {128, 1,
+// box_rows, 1} (one 128-byte row per sequence position when D = 128).
+inline bool make_bshd_map_e4m3(CUtensorMap* map, const void* ptr, int B, int L, int heads, int D,
+                               int box_rows = 128) {
+  EncodeTiledFn fn = encode_tiled_fn();
+  if (!fn) return false;
+  cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)heads, (cuuint64_t)L, (cuuint64_t)B};
+  cuuint64_t strides[3] = {(cuuint64_t)D, (cuuint64_t)heads * D, (cuuint64_t)L * heads * D};
+  cuuint32_t box[4] = {128, 1, (cuuint32_t)box_rows, 1};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, const_cast<void*>(ptr), dims, strides, box,
+                  estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 inline int sm_count() {
   int dev = 0, n = 0;
   cudaGetDevice(&dev);

@@ -1,4 +1,5 @@
 // Host launcher of the forward kernel.
+#include <cmath>
 #include <type_traits>
 
 #include "common.cuh"
@@ -7,14 +8,23 @@
 
 namespace fa {
 
-template <int D, bool BF16>
+// FP8: Q, K, V are E4M3 codes with per-tensor scales qs, ks, vs; BF16 then
+// selects the output type.
+template <int D, bool BF16, bool FP8 = false>
 static fa_status launch(const void* Q, const void* K, const void* V, void* O, float* LSE, int B,
-                        int Lq, int Lk, int H, int Hkv, int causal, cudaStream_t s) {
-  using Ly = FwdLayout<D>;
+                        int Lq, int Lk, int H, int Hkv, int causal, cudaStream_t s, float qs = 1.f,
+                        float ks = 1.f, float vs = 1.f) {
+  using Ly = FwdLayout<D, FP8>;
   CUtensorMap tq, tk, tv;
-  if (!make_bshd_map(&tq, Q, B, Lq, H, D, BF16) || !make_bshd_map(&tk, K, B, Lk, Hkv, D, BF16) ||
-      !make_bshd_map(&tv, V, B, Lk, Hkv, D, BF16))
-    return FA_ERR_CUDA;
+  if constexpr (FP8) {
+    if (!make_bshd_map_e4m3(&tq, Q, B, Lq, H, D) || !make_bshd_map_e4m3(&tk, K, B, Lk, Hkv, D) ||
+        !make_bshd_map_e4m3(&tv, V, B, Lk, Hkv, D))
+      return FA_ERR_CUDA;
+  } else {
+    if (!make_bshd_map(&tq, Q, B, Lq, H, D, BF16) || !make_bshd_map(&tk, K, B, Lk, Hkv, D, BF16) ||
+        !make_bshd_map(&tv, V, B, Lk, Hkv, D, BF16))
+      return FA_ERR_CUDA;
+  }
   FwdParams p;
   p.O = O;
   p.LSE = LSE;
@@ -28,8 +38,13 @@ static fa_status launch(const void* Q, const void* K, const void* V, void* O, fl
   p.n_kv = (Lk + 127) / 128;
   p.n_qpairs = (Lq + 255) / 256;
   p.n_items = B * H * p.n_qpairs;
-  p.sl2 = 1.4426950408889634f / sqrtf(static_cast<float>(D));
-  auto kern = fa_fwd_kernel<D, BF16>;
+  // Scores carry q_scale * k_scale (1 for 16-bit inputs); v_scale is applied
+  // with 1 / l at the store.
+  p.sl2 = FP8 ? static_cast<float>(1.4426950408889634 * static_cast<double>(qs) *
+                                   static_cast<double>(ks) / std::sqrt(static_cast<double>(D)))
+              : 1.4426950408889634f / sqrtf(static_cast<float>(D));
+  p.o_scale = vs;
+  auto kern = fa_fwd_kernel<D, BF16, FP8>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Ly::SMEM_ALLOC) !=
       cudaSuccess)
     return FA_ERR_CUDA;
@@ -47,6 +62,16 @@ fa_status run_fwd(const void* Q, const void* K, const void* V, void* O, float* L
   }
   return bf16 ? launch<128, true>(Q, K, V, O, LSE, B, Lq, Lk, H, Hkv, causal, s)
               : launch<128, false>(Q, K, V, O, LSE, B, Lq, Lk, H, Hkv, causal, s);
+}
+
+fa_status run_fwd_fp8(const void* Q8, const void* K8, const void* V8, float q_scale, float k_scale,
+                      float v_scale, void* O, float* LSE, int B, int Lq, int Lk, int H, int Hkv,
+                      int causal, int out_dtype, cudaStream_t s) {
+  return out_dtype == FA_BF16
+             ? launch<128, true, true>(Q8, K8, V8, O, LSE, B, Lq, Lk, H, Hkv, causal, s, q_scale,
+                                       k_scale, v_scale)
+             : launch<128, false, true>(Q8, K8, V8, O, LSE, B, Lq, Lk, H, Hkv, causal, s, q_scale,
+                                        k_scale, v_scale);
 }
 
 unsigned int fwd_read_error(cudaStream_t s) { return read_and_clear_error(s); }

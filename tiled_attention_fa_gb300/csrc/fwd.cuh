@@ -42,15 +42,22 @@ struct FwdParams {
   int n_kv;      // ceil(Lk / 128)
   int n_qpairs;  // ceil(Lq / 256)
   int n_items;   // B * H * n_qpairs
-  float sl2;     // log2(e) / sqrt(D)
+  float sl2;     // log2(e) / sqrt(D) (times q_scale * k_scale for E4M3 inputs)
+  float o_scale; // factor on O / l at the store: 1, or v_scale for E4M3 inputs
 };
 
-template <int D>
+// FP8: Q, K, V are E4M3 codes (one byte per element; D = 128 only).
+template <int D, bool FP8 = false>
 struct FwdLayout {
-  static constexpr int KCH = D / 64;              // 128-byte column chunks per row
+  static constexpr int EB = FP8 ? 1 : 2;          // bytes per input element
+  static constexpr int KCH = D * EB / 128;        // 128-byte column chunks per row
   static constexpr uint32_t CHUNK = 128u * 128u;  // 128 rows x 128 B
   static constexpr uint32_t TILE = KCH * CHUNK;   // one 128 x D tile
-  static constexpr int STAGES = (D == 128) ? 4 : 8;
+  static constexpr int STAGES = FP8 ? 10 : ((D == 128) ? 4 : 8);
+  static constexpr int KS_S = D * EB / 32;        // MMA steps of S = Q K^T (32 bytes of K each)
+  static constexpr int KS_PV = 4 * EB;            // MMA steps of O += P V (32 / EB keys each)
+  static constexpr uint32_t V_STEP = (32 / EB) * 128u;  // V bytes per PV step
+  static_assert(!FP8 || D == 128, "E4M3 inputs need D = 128");
   static constexpr uint32_t Q_OFF = 0;
   static constexpr uint32_t RING_OFF = 2 * TILE;
   static constexpr uint32_t BAR_OFF = RING_OFF + STAGES * TILE;
@@ -112,14 +119,16 @@ __device__ __forceinline__ uint32_t pack2<__nv_bfloat16>(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
-template <int D, bool BF16>
+template <int D, bool BF16, bool FP8 = false>
 __global__ void __launch_bounds__(320, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const FwdParams p) {
-  using Ly = FwdLayout<D>;
+  using Ly = FwdLayout<D, FP8>;
   using T = typename std::conditional<BF16, __nv_bfloat16, __half>::type;
-  constexpr uint32_t IDESC_S = idesc_f16(BF16, 128, 128, false, false);
-  constexpr uint32_t IDESC_PV = idesc_f16(BF16, 128, D, false, true);
+  // Operand formats: F16 = 0 / BF16 = 1 for 16-bit inputs; E4M3 = 0 under
+  // .kind::f8f6f4 (BF16 then only selects the output type).
+  constexpr uint32_t IDESC_S = idesc_f16(BF16 && !FP8, 128, 128, false, false);
+  constexpr uint32_t IDESC_PV = idesc_f16(BF16 && !FP8, 128, D, false, true);
 
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
@@ -184,7 +193,7 @@ __global__ void __launch_bounds__(320, 1)
         for (int t = 0; t < 2; ++t)
           for (int c = 0; c < Ly::KCH; ++c)
             tma_load_4d(base + Ly::Q_OFF + t * Ly::TILE + c * Ly::CHUNK, &tmQ, bar(Ly::B_QFULL),
-                        c * 64, it.h, it.q0 + 128 * t, it.b);
+                        c * (128 / Ly::EB), it.h, it.q0 + 128 * t, it.b);
         ++q_uses;
         const int nmax = max(it.n[0], it.n[1]);
         for (int j = 0; ok && j < nmax; ++j) {
@@ -197,7 +206,8 @@ __global__ void __launch_bounds__(320, 1)
             const CUtensorMap* m = kv ? &tmV : &tmK;
             for (int c = 0; c < Ly::KCH; ++c)
               tma_load_4d_hint(base + Ly::RING_OFF + stage * Ly::TILE + c * Ly::CHUNK, m,
-                               bar(Ly::B_KVFULL + stage), c * 64, it.hkv, j * 128, it.b, keep);
+                               bar(Ly::B_KVFULL + stage), c * (128 / Ly::EB), it.hkv, j * 128, it.b,
+                               keep);
             ++issued[stage];
             if (++stage == Ly::STAGES) {
               stage = 0;
@@ -226,18 +236,27 @@ __global__ void __launch_bounds__(320, 1)
         const uint32_t qa = base + Ly::Q_OFF + t * Ly::TILE;
         const uint32_t ka = base + Ly::RING_OFF + kslot * Ly::TILE;
 #pragma unroll
-        for (int k = 0; k < D / 16; ++k) {
+        for (int k = 0; k < Ly::KS_S; ++k) {
           const uint32_t off = (k >> 2) * Ly::CHUNK + (k & 3) * 32u;
-          mma_ss(tS[t], sdesc_sw128(qa + off, 16, 1024), sdesc_sw128(ka + off, 16, 1024), IDESC_S,
-                 k > 0 ? 1u : 0u);
+          if constexpr (FP8)
+            mma_ss_f8(tS[t], sdesc_sw128(qa + off, 16, 1024), sdesc_sw128(ka + off, 16, 1024),
+                      IDESC_S, k > 0 ? 1u : 0u);
+          else
+            mma_ss(tS[t], sdesc_sw128(qa + off, 16, 1024), sdesc_sw128(ka + off, 16, 1024), IDESC_S,
+                   k > 0 ? 1u : 0u);
         }
       };
       auto issue_pv = [&](int t, uint32_t vslot, bool acc) {
         const uint32_t va = base + Ly::RING_OFF + vslot * Ly::TILE;
 #pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          mma_ts(tO[t], tS[t] + 8u * k, sdesc_sw128(va + 2048u * k, Ly::CHUNK, 1024), IDESC_PV,
-                 (acc || k > 0) ? 1u : 0u);
+        for (int k = 0; k < Ly::KS_PV; ++k) {
+          // P: 8 TMEM columns (16 or 32 keys) per step; V read MN-major.
+          if constexpr (FP8)
+            mma_ts_f8(tO[t], tS[t] + 8u * k, sdesc_sw128(va + Ly::V_STEP * k, Ly::CHUNK, 1024),
+                      IDESC_PV, (acc || k > 0) ? 1u : 0u);
+          else
+            mma_ts(tO[t], tS[t] + 8u * k, sdesc_sw128(va + Ly::V_STEP * k, Ly::CHUNK, 1024),
+                   IDESC_PV, (acc || k > 0) ? 1u : 0u);
         }
       };
       auto take = [&](uint32_t& slot, unsigned int site) -> bool {
@@ -368,17 +387,36 @@ __global__ void __launch_bounds__(320, 1)
         }
         const float mb = m * sl2;
         float rs = 0.f;
+        if constexpr (FP8) {
+          // P as E4M3, four keys per TMEM column (32 columns per tile).
 #pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4) {
-          uint32_t pk[16];
+          for (int h2 = 0; h2 < 2; ++h2) {
+            uint32_t pk[16];
 #pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            const float p0 = ex2(fmaf(__uint_as_float(sr[32 * q4 + 2 * i]), sl2, -mb));
-            const float p1 = ex2(fmaf(__uint_as_float(sr[32 * q4 + 2 * i + 1]), sl2, -mb));
-            rs += p0 + p1;
-            pk[i] = pack2<T>(p0, p1);
+            for (int i = 0; i < 16; ++i) {
+              const int c = 64 * h2 + 4 * i;
+              const float p0 = ex2(fmaf(__uint_as_float(sr[c]), sl2, -mb));
+              const float p1 = ex2(fmaf(__uint_as_float(sr[c + 1]), sl2, -mb));
+              const float p2 = ex2(fmaf(__uint_as_float(sr[c + 2]), sl2, -mb));
+              const float p3 = ex2(fmaf(__uint_as_float(sr[c + 3]), sl2, -mb));
+              rs += (p0 + p1) + (p2 + p3);
+              pk[i] = pack4_e4m3(p0, p1, p2, p3);
+            }
+            tmem_st16(tS + 16 * h2, pk);
           }
-          tmem_st16(tS + 16 * q4, pk);
+        } else {
+#pragma unroll
+          for (int q4 = 0; q4 < 4; ++q4) {
+            uint32_t pk[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              const float p0 = ex2(fmaf(__uint_as_float(sr[32 * q4 + 2 * i]), sl2, -mb));
+              const float p1 = ex2(fmaf(__uint_as_float(sr[32 * q4 + 2 * i + 1]), sl2, -mb));
+              rs += p0 + p1;
+              pk[i] = pack2<T>(p0, p1);
+            }
+            tmem_st16(tS + 16 * q4, pk);
+          }
         }
         if (rescale) {
           // O of this row scaled by alpha.  PV of the previous tile has
@@ -403,7 +441,7 @@ __global__ void __launch_bounds__(320, 1)
       if (!mbar_wait_warp(bar(Ly::B_OFULL + t), o_cnt & 1, ab, err, 302)) { ok = false; break; }
       ++o_cnt;
       tc_fence_after();
-      const float inv = l > 0.f ? 1.f / l : 0.f;
+      const float inv = l > 0.f ? p.o_scale / l : 0.f;
       T* orow = reinterpret_cast<T*>(p.O) + ((static_cast<size_t>(it.b) * p.Lq + q) * p.H + it.h) * D;
 #pragma unroll
       for (int cc = 0; cc < D / 32; ++cc) {

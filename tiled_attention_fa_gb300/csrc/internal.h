@@ -9,6 +9,9 @@ namespace fa {
 
 fa_status run_fwd(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int Lq,
                   int Lk, int H, int Hkv, int D, int causal, int dtype, cudaStream_t s);
+fa_status run_fwd_fp8(const void* Q8, const void* K8, const void* V8, float q_scale, float k_scale,
+                      float v_scale, void* O, float* LSE, int B, int Lq, int Lk, int H, int Hkv,
+                      int causal, int out_dtype, cudaStream_t s);
 unsigned int fwd_read_error(cudaStream_t s);
 fa_status run_selftest_wait(unsigned long long limit_ns, cudaStream_t s);
 
