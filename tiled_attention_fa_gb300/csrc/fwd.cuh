@@ -361,38 +361,24 @@ __global__ void __launch_bounds__(320, 1)
         tmem_ld_wait32(sr + 96);
         const int k0 = j * 128;
         const bool need_mask = (k0 + 128 > p.Lk) || (p.causal && k0 + 127 > tile_lo + p.past);
-        float mx = -INFINITY;
-        if constexpr (FP8) {
-          if (need_mask) {
-            const int lim = p.causal ? min(q + p.past + 1, p.Lk) : p.Lk;  // keys [0, lim) visible
-#pragma unroll
-            for (int c = 0; c < 128; ++c)
-              if (k0 + c >= lim) sr[c] = __float_as_uint(-INFINITY);
-          }
-          // E4M3 halves the MMA time per tile, so the softmax sets the pace:
-          // the row max runs as four independent chains of three-input max
-          // operations (key 4t+u in chain u) instead of 128 dependent ones.
-          float mx4[4];
-#pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            mx4[u] = __uint_as_float(sr[u]);
-#pragma unroll
-            for (int t = 1; t < 31; t += 2)
-              mx4[u] = fmax3(mx4[u], __uint_as_float(sr[4 * t + u]), __uint_as_float(sr[4 * t + 4 + u]));
-            mx4[u] = fmaxf(mx4[u], __uint_as_float(sr[124 + u]));
-          }
-          mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
-        } else if (need_mask) {
+        if (need_mask) {
           const int lim = p.causal ? min(q + p.past + 1, p.Lk) : p.Lk;  // keys [0, lim) visible
 #pragma unroll
-          for (int c = 0; c < 128; ++c) {
+          for (int c = 0; c < 128; ++c)
             if (k0 + c >= lim) sr[c] = __float_as_uint(-INFINITY);
-            mx = fmaxf(mx, __uint_as_float(sr[c]));
-          }
-        } else {
-#pragma unroll
-          for (int c = 0; c < 128; ++c) mx = fmaxf(mx, __uint_as_float(sr[c]));
         }
+        // The row max runs as four independent chains of three-input max
+        // operations (key 4w+u in chain u) instead of 128 dependent ones.
+        float mx4[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          mx4[u] = __uint_as_float(sr[u]);
+#pragma unroll
+          for (int w = 1; w < 31; w += 2)
+            mx4[u] = fmax3(mx4[u], __uint_as_float(sr[4 * w + u]), __uint_as_float(sr[4 * w + 4 + u]));
+          mx4[u] = fmaxf(mx4[u], __uint_as_float(sr[124 + u]));
+        }
+        const float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
         const float m_new = fmaxf(m, mx);
         float alpha = 1.f;
         bool rescale = false;
@@ -437,18 +423,32 @@ __global__ void __launch_bounds__(320, 1)
           }
           rs = (rs4[0] + rs4[1]) + (rs4[2] + rs4[3]);
         } else {
+          // Exponent arguments and the row sum on paired fp32 instructions
+          // (two keys per FMA / ADD), the sum over four independent pairs.
+          const uint64_t sl2x2 = f2_pack(sl2, sl2), nmb2 = f2_pack(-mb, -mb);
+          uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};
 #pragma unroll
           for (int q4 = 0; q4 < 4; ++q4) {
             uint32_t pk[16];
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
-              const float p0 = ex2(fmaf(__uint_as_float(sr[32 * q4 + 2 * i]), sl2, -mb));
-              const float p1 = ex2(fmaf(__uint_as_float(sr[32 * q4 + 2 * i + 1]), sl2, -mb));
-              rs += p0 + p1;
+              const int c = 32 * q4 + 2 * i;
+              float a0, a1;
+              f2_unpack(ffma2(f2_pack(__uint_as_float(sr[c]), __uint_as_float(sr[c + 1])), sl2x2, nmb2), a0, a1);
+              const float p0 = ex2(a0), p1 = ex2(a1);
+              acc[i & 3] = fadd2(acc[i & 3], f2_pack(p0, p1));
               pk[i] = pack2<T>(p0, p1);
             }
             tmem_st16(tS + 16 * q4, pk);
           }
+          float rs4[4];
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            float lo, hi;
+            f2_unpack(acc[u], lo, hi);
+            rs4[u] = lo + hi;
+          }
+          rs = (rs4[0] + rs4[1]) + (rs4[2] + rs4[3]);
         }
         if (rescale) {
           // O of this row scaled by alpha.  PV of the previous tile has
