@@ -225,43 +225,55 @@ __global__ void __launch_bounds__(320, 1)
     }
   } else if (warp == 9) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+    // The whole warp runs the schedule, so loop state and operand descriptors
+    // are warp-uniform values; one elected lane issues each MMA group and the
+    // commits that track it.
+    {
       uint32_t stage = 0, phase = 0, q_cnt = 0;
       uint32_t p_cnt[2] = {0, 0}, o_uses[2] = {0, 0};
       bool ok = true;
       const uint32_t tS[2] = {tmem + Ly::TM_S0, tmem + Ly::TM_S1};
       const uint32_t tO[2] = {tmem + Ly::TM_O0, tmem + Ly::TM_O1};
+      auto commit = [&](int b) {
+        if (elect_one()) tc_commit(bar(b));
+        __syncwarp();
+      };
 
+      // Descriptors of the first K step; later steps add their byte offset
+      // (>> 4) to the start-address field, which stays below 2^14.
       auto issue_s = [&](int t, uint32_t kslot) {
-        const uint32_t qa = base + Ly::Q_OFF + t * Ly::TILE;
-        const uint32_t ka = base + Ly::RING_OFF + kslot * Ly::TILE;
+        const uint64_t qd = sdesc_sw128(base + Ly::Q_OFF + t * Ly::TILE, 16, 1024);
+        const uint64_t kd = sdesc_sw128(base + Ly::RING_OFF + kslot * Ly::TILE, 16, 1024);
+        if (elect_one()) {
 #pragma unroll
-        for (int k = 0; k < Ly::KS_S; ++k) {
-          const uint32_t off = (k >> 2) * Ly::CHUNK + (k & 3) * 32u;
-          if constexpr (FP8)
-            mma_ss_f8(tS[t], sdesc_sw128(qa + off, 16, 1024), sdesc_sw128(ka + off, 16, 1024),
-                      IDESC_S, k > 0 ? 1u : 0u);
-          else
-            mma_ss(tS[t], sdesc_sw128(qa + off, 16, 1024), sdesc_sw128(ka + off, 16, 1024), IDESC_S,
-                   k > 0 ? 1u : 0u);
+          for (int k = 0; k < Ly::KS_S; ++k) {
+            const uint64_t off = ((k >> 2) * Ly::CHUNK + (k & 3) * 32u) >> 4;
+            if constexpr (FP8)
+              mma_ss_f8(tS[t], qd + off, kd + off, IDESC_S, k > 0 ? 1u : 0u);
+            else
+              mma_ss(tS[t], qd + off, kd + off, IDESC_S, k > 0 ? 1u : 0u);
+          }
         }
+        __syncwarp();
       };
       auto issue_pv = [&](int t, uint32_t vslot, bool acc) {
-        const uint32_t va = base + Ly::RING_OFF + vslot * Ly::TILE;
+        const uint64_t vd = sdesc_sw128(base + Ly::RING_OFF + vslot * Ly::TILE, Ly::CHUNK, 1024);
+        if (elect_one()) {
 #pragma unroll
-        for (int k = 0; k < Ly::KS_PV; ++k) {
-          // P: 8 TMEM columns (16 or 32 keys) per step; V read MN-major.
-          if constexpr (FP8)
-            mma_ts_f8(tO[t], tS[t] + 8u * k, sdesc_sw128(va + Ly::V_STEP * k, Ly::CHUNK, 1024),
-                      IDESC_PV, (acc || k > 0) ? 1u : 0u);
-          else
-            mma_ts(tO[t], tS[t] + 8u * k, sdesc_sw128(va + Ly::V_STEP * k, Ly::CHUNK, 1024),
-                   IDESC_PV, (acc || k > 0) ? 1u : 0u);
+          for (int k = 0; k < Ly::KS_PV; ++k) {
+            // P: 8 TMEM columns (16 or 32 keys) per step; V read MN-major.
+            const uint64_t off = (Ly::V_STEP * k) >> 4;
+            if constexpr (FP8)
+              mma_ts_f8(tO[t], tS[t] + 8u * k, vd + off, IDESC_PV, (acc || k > 0) ? 1u : 0u);
+            else
+              mma_ts(tO[t], tS[t] + 8u * k, vd + off, IDESC_PV, (acc || k > 0) ? 1u : 0u);
+          }
         }
+        __syncwarp();
       };
       auto take = [&](uint32_t& slot, unsigned int site) -> bool {
         slot = stage;
-        if (!mbar_wait(bar(Ly::B_KVFULL + stage), phase, ab, err, site)) return false;
+        if (!mbar_wait_warp(bar(Ly::B_KVFULL + stage), phase, ab, err, site)) return false;
         if (++stage == Ly::STAGES) {
           stage = 0;
           phase ^= 1u;
@@ -275,7 +287,7 @@ __global__ void __launch_bounds__(320, 1)
         if (item >= p.n_items) continue;
         const FwdItem it = fwd_decode(item, p);
         const int nmax = max(it.n[0], it.n[1]);
-        if (!mbar_wait(bar(Ly::B_QFULL), q_cnt & 1, ab, err, 201)) { ok = false; break; }
+        if (!mbar_wait_warp(bar(Ly::B_QFULL), q_cnt & 1, ab, err, 201)) { ok = false; break; }
         ++q_cnt;
         tc_fence_after();
         uint32_t kslot;
@@ -283,9 +295,9 @@ __global__ void __launch_bounds__(320, 1)
         for (int t = 0; t < 2; ++t)
           if (it.n[t] > 0) {
             issue_s(t, kslot);
-            tc_commit(bar(Ly::B_SFULL + t));
+            commit(Ly::B_SFULL + t);
           }
-        tc_commit(bar(Ly::B_KVEMPTY + kslot));
+        commit(Ly::B_KVEMPTY + kslot);
         for (int j = 0; ok && j < nmax; ++j) {
           uint32_t vslot, kslot1 = 0;
           bool k_ready = false;
@@ -293,16 +305,19 @@ __global__ void __launch_bounds__(320, 1)
           for (int t = 0; t < 2; ++t) {
             if (j < it.n[t]) {
               if (j == 0 && o_uses[t] > 0 &&
-                  !mbar_wait(bar(Ly::B_OEMPTY + t), (o_uses[t] - 1) & 1, ab, err, 204)) {
+                  !mbar_wait_warp(bar(Ly::B_OEMPTY + t), (o_uses[t] - 1) & 1, ab, err, 204)) {
                 ok = false;
                 break;
               }
-              if (!mbar_wait(bar(Ly::B_PFULL + t), p_cnt[t] & 1, ab, err, 205)) { ok = false; break; }
+              if (!mbar_wait_warp(bar(Ly::B_PFULL + t), p_cnt[t] & 1, ab, err, 205)) {
+                ok = false;
+                break;
+              }
               ++p_cnt[t];
               tc_fence_after();
               issue_pv(t, vslot, j > 0);
               if (j == it.n[t] - 1) {
-                tc_commit(bar(Ly::B_OFULL + t));
+                commit(Ly::B_OFULL + t);
                 ++o_uses[t];
               }
             }
@@ -312,18 +327,18 @@ __global__ void __launch_bounds__(320, 1)
                 k_ready = true;
               }
               issue_s(t, kslot1);
-              tc_commit(bar(Ly::B_SFULL + t));
+              commit(Ly::B_SFULL + t);
             }
           }
           if (!ok) break;
-          tc_commit(bar(Ly::B_KVEMPTY + vslot));
-          if (k_ready) tc_commit(bar(Ly::B_KVEMPTY + kslot1));
+          commit(Ly::B_KVEMPTY + vslot);
+          if (k_ready) commit(Ly::B_KVEMPTY + kslot1);
         }
         if (!ok) break;
-        tc_commit(bar(Ly::B_QEMPTY));
+        commit(Ly::B_QEMPTY);
       }
-      // Every MMA issued by this thread completes before TMEM is released.
-      tc_commit(bar(Ly::B_DONE));
+      // Every MMA issued by the elected lane completes before TMEM is released.
+      commit(Ly::B_DONE);
       mbar_wait_drain(bar(Ly::B_DONE), 0);
     }
   }
