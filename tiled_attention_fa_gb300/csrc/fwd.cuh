@@ -12,7 +12,7 @@
 // GB300 design (not the page's): one persistent CTA per SM, 320 threads.
 //   warps 0-3  softmax warpgroup for Q tile 0 (thread i owns row i)
 //   warps 4-7  softmax warpgroup for Q tile 1
-//   warp  8    TMA producer: Q pair, then K_j, V_j into a ring of smem slots
+//   warp  8    TMA producer: Q pair, then (V_{j-1}, K_j) tile pairs into a ring
 //   warp  9    TMEM allocator and the single tcgen05.mma issuing thread
 // Registers are not re-balanced between warps (no setmaxnreg): a fixed split
 // depends on the launch allocation and would wait forever if a tool or
@@ -53,14 +53,16 @@ struct FwdLayout {
   static constexpr int KCH = D * EB / 128;        // 128-byte column chunks per row
   static constexpr uint32_t CHUNK = 128u * 128u;  // 128 rows x 128 B
   static constexpr uint32_t TILE = KCH * CHUNK;   // one 128 x D tile
-  static constexpr int STAGES = FP8 ? 10 : ((D == 128) ? 4 : 8);
+  // Ring stages, each holding a pair of tiles: (V_{j-1}, K_j), the tiles one
+  // step of the MMA schedule consumes (V_{j-1} for P V, K_j for the next S).
+  static constexpr int STAGES = FP8 ? 5 : ((D == 128) ? 2 : 4);
   static constexpr int KS_S = D * EB / 32;        // MMA steps of S = Q K^T (32 bytes of K each)
   static constexpr int KS_PV = 4 * EB;            // MMA steps of O += P V (32 / EB keys each)
   static constexpr uint32_t V_STEP = (32 / EB) * 128u;  // V bytes per PV step
   static_assert(!FP8 || D == 128, "E4M3 inputs need D = 128");
   static constexpr uint32_t Q_OFF = 0;
   static constexpr uint32_t RING_OFF = 2 * TILE;
-  static constexpr uint32_t BAR_OFF = RING_OFF + STAGES * TILE;
+  static constexpr uint32_t BAR_OFF = RING_OFF + STAGES * 2 * TILE;
   // barrier slots
   static constexpr int B_QFULL = 0, B_QEMPTY = 1, B_KVFULL = 2, B_KVEMPTY = 2 + STAGES,
                        B_SFULL = 2 + 2 * STAGES, B_PFULL = B_SFULL + 2, B_OFULL = B_PFULL + 2,
@@ -150,9 +152,9 @@ __global__ void __launch_bounds__(320, 1)
     }
     for (int t = 0; t < 2; ++t) {
       mbar_init(bar(Ly::B_SFULL + t), 1);
-      mbar_init(bar(Ly::B_PFULL + t), 128);
+      mbar_init(bar(Ly::B_PFULL + t), 4);  // one arrival per warp of the warpgroup
       mbar_init(bar(Ly::B_OFULL + t), 1);
-      mbar_init(bar(Ly::B_OEMPTY + t), 128);
+      mbar_init(bar(Ly::B_OEMPTY + t), 4);
     }
     mbar_init(bar(Ly::B_DONE), 1);
     ab->flag = 0;
@@ -196,23 +198,27 @@ __global__ void __launch_bounds__(320, 1)
                         c * (128 / Ly::EB), it.h, it.q0 + 128 * t, it.b);
         ++q_uses;
         const int nmax = max(it.n[0], it.n[1]);
-        for (int j = 0; ok && j < nmax; ++j) {
-          for (int kv = 0; kv < 2; ++kv) {
-            if (!mbar_wait(bar(Ly::B_KVEMPTY + stage), phase ^ 1u, ab, err, 102)) {
-              ok = false;
-              break;
-            }
-            mbar_arrive_expect_tx(bar(Ly::B_KVFULL + stage), Ly::TILE);
-            const CUtensorMap* m = kv ? &tmV : &tmK;
-            for (int c = 0; c < Ly::KCH; ++c)
-              tma_load_4d_hint(base + Ly::RING_OFF + stage * Ly::TILE + c * Ly::CHUNK, m,
-                               bar(Ly::B_KVFULL + stage), c * (128 / Ly::EB), it.hkv, j * 128, it.b,
-                               keep);
-            ++issued[stage];
-            if (++stage == Ly::STAGES) {
-              stage = 0;
-              phase ^= 1u;
-            }
+        // Pair j = (V_{j-1}, K_j): the first has no V, the last no K.
+        for (int j = 0; ok && j <= nmax; ++j) {
+          if (!mbar_wait(bar(Ly::B_KVEMPTY + stage), phase ^ 1u, ab, err, 102)) {
+            ok = false;
+            break;
+          }
+          const uint32_t slot = base + Ly::RING_OFF + stage * 2 * Ly::TILE;
+          mbar_arrive_expect_tx(bar(Ly::B_KVFULL + stage),
+                                ((j > 0 ? 1u : 0u) + (j < nmax ? 1u : 0u)) * Ly::TILE);
+          for (int c = 0; c < Ly::KCH; ++c) {
+            if (j > 0)
+              tma_load_4d_hint(slot + c * Ly::CHUNK, &tmV, bar(Ly::B_KVFULL + stage),
+                               c * (128 / Ly::EB), it.hkv, (j - 1) * 128, it.b, keep);
+            if (j < nmax)
+              tma_load_4d_hint(slot + Ly::TILE + c * Ly::CHUNK, &tmK, bar(Ly::B_KVFULL + stage),
+                               c * (128 / Ly::EB), it.hkv, j * 128, it.b, keep);
+          }
+          ++issued[stage];
+          if (++stage == Ly::STAGES) {
+            stage = 0;
+            phase ^= 1u;
           }
         }
       }
@@ -230,10 +236,11 @@ __global__ void __launch_bounds__(320, 1)
     // commits that track it.
     {
       uint32_t stage = 0, phase = 0, q_cnt = 0;
-      uint32_t p_cnt[2] = {0, 0}, o_uses[2] = {0, 0};
+      // Per-tile counters of P hand-offs and O uses, kept in registers.
+      uint32_t p_cnt0 = 0, p_cnt1 = 0, o_uses0 = 0, o_uses1 = 0;
       bool ok = true;
-      const uint32_t tS[2] = {tmem + Ly::TM_S0, tmem + Ly::TM_S1};
-      const uint32_t tO[2] = {tmem + Ly::TM_O0, tmem + Ly::TM_O1};
+      auto tS = [&](int t) { return tmem + Ly::TM_S0 + (Ly::TM_S1 - Ly::TM_S0) * t; };
+      auto tO = [&](int t) { return tmem + Ly::TM_O0 + (Ly::TM_O1 - Ly::TM_O0) * t; };
       auto commit = [&](int b) {
         if (elect_one()) tc_commit(bar(b));
         __syncwarp();
@@ -241,32 +248,34 @@ __global__ void __launch_bounds__(320, 1)
 
       // Descriptors of the first K step; later steps add their byte offset
       // (>> 4) to the start-address field, which stays below 2^14.
-      auto issue_s = [&](int t, uint32_t kslot) {
+      // K of pair `ps` is its second tile, V its first.
+      auto issue_s = [&](int t, uint32_t ps) {
         const uint64_t qd = sdesc_sw128(base + Ly::Q_OFF + t * Ly::TILE, 16, 1024);
-        const uint64_t kd = sdesc_sw128(base + Ly::RING_OFF + kslot * Ly::TILE, 16, 1024);
+        const uint64_t kd =
+            sdesc_sw128(base + Ly::RING_OFF + (2 * ps + 1) * Ly::TILE, 16, 1024);
         if (elect_one()) {
 #pragma unroll
           for (int k = 0; k < Ly::KS_S; ++k) {
             const uint64_t off = ((k >> 2) * Ly::CHUNK + (k & 3) * 32u) >> 4;
             if constexpr (FP8)
-              mma_ss_f8(tS[t], qd + off, kd + off, IDESC_S, k > 0 ? 1u : 0u);
+              mma_ss_f8(tS(t), qd + off, kd + off, IDESC_S, k > 0 ? 1u : 0u);
             else
-              mma_ss(tS[t], qd + off, kd + off, IDESC_S, k > 0 ? 1u : 0u);
+              mma_ss(tS(t), qd + off, kd + off, IDESC_S, k > 0 ? 1u : 0u);
           }
         }
         __syncwarp();
       };
-      auto issue_pv = [&](int t, uint32_t vslot, bool acc) {
-        const uint64_t vd = sdesc_sw128(base + Ly::RING_OFF + vslot * Ly::TILE, Ly::CHUNK, 1024);
+      auto issue_pv = [&](int t, uint32_t ps, bool acc) {
+        const uint64_t vd = sdesc_sw128(base + Ly::RING_OFF + 2 * ps * Ly::TILE, Ly::CHUNK, 1024);
         if (elect_one()) {
 #pragma unroll
           for (int k = 0; k < Ly::KS_PV; ++k) {
             // P: 8 TMEM columns (16 or 32 keys) per step; V read MN-major.
             const uint64_t off = (Ly::V_STEP * k) >> 4;
             if constexpr (FP8)
-              mma_ts_f8(tO[t], tS[t] + 8u * k, vd + off, IDESC_PV, (acc || k > 0) ? 1u : 0u);
+              mma_ts_f8(tO(t), tS(t) + 8u * k, vd + off, IDESC_PV, (acc || k > 0) ? 1u : 0u);
             else
-              mma_ts(tO[t], tS[t] + 8u * k, vd + off, IDESC_PV, (acc || k > 0) ? 1u : 0u);
+              mma_ts(tO(t), tS(t) + 8u * k, vd + off, IDESC_PV, (acc || k > 0) ? 1u : 0u);
           }
         }
         __syncwarp();
@@ -290,49 +299,48 @@ __global__ void __launch_bounds__(320, 1)
         if (!mbar_wait_warp(bar(Ly::B_QFULL), q_cnt & 1, ab, err, 201)) { ok = false; break; }
         ++q_cnt;
         tc_fence_after();
-        uint32_t kslot;
-        if (!take(kslot, 202)) { ok = false; break; }
+        // Pair 0 holds K_0: the first S of both tiles.
+        uint32_t ps;
+        if (!take(ps, 202)) { ok = false; break; }
+#pragma unroll
         for (int t = 0; t < 2; ++t)
           if (it.n[t] > 0) {
-            issue_s(t, kslot);
+            issue_s(t, ps);
             commit(Ly::B_SFULL + t);
           }
-        commit(Ly::B_KVEMPTY + kslot);
+        commit(Ly::B_KVEMPTY + ps);
         for (int j = 0; ok && j < nmax; ++j) {
-          uint32_t vslot, kslot1 = 0;
-          bool k_ready = false;
-          if (!take(vslot, 203)) { ok = false; break; }
+          // Pair j+1 holds V_j and K_{j+1}.
+          if (!take(ps, 203)) { ok = false; break; }
+#pragma unroll
           for (int t = 0; t < 2; ++t) {
+            uint32_t& p_cnt = t ? p_cnt1 : p_cnt0;
+            uint32_t& o_uses = t ? o_uses1 : o_uses0;
             if (j < it.n[t]) {
-              if (j == 0 && o_uses[t] > 0 &&
-                  !mbar_wait_warp(bar(Ly::B_OEMPTY + t), (o_uses[t] - 1) & 1, ab, err, 204)) {
+              if (j == 0 && o_uses > 0 &&
+                  !mbar_wait_warp(bar(Ly::B_OEMPTY + t), (o_uses - 1) & 1, ab, err, 204)) {
                 ok = false;
                 break;
               }
-              if (!mbar_wait_warp(bar(Ly::B_PFULL + t), p_cnt[t] & 1, ab, err, 205)) {
+              if (!mbar_wait_warp(bar(Ly::B_PFULL + t), p_cnt & 1, ab, err, 205)) {
                 ok = false;
                 break;
               }
-              ++p_cnt[t];
+              ++p_cnt;
               tc_fence_after();
-              issue_pv(t, vslot, j > 0);
+              issue_pv(t, ps, j > 0);
               if (j == it.n[t] - 1) {
                 commit(Ly::B_OFULL + t);
-                ++o_uses[t];
+                ++o_uses;
               }
             }
             if (j + 1 < it.n[t]) {
-              if (!k_ready) {
-                if (!take(kslot1, 206)) { ok = false; break; }
-                k_ready = true;
-              }
-              issue_s(t, kslot1);
+              issue_s(t, ps);
               commit(Ly::B_SFULL + t);
             }
           }
           if (!ok) break;
-          commit(Ly::B_KVEMPTY + vslot);
-          if (k_ready) commit(Ly::B_KVEMPTY + kslot1);
+          commit(Ly::B_KVEMPTY + ps);
         }
         if (!ok) break;
         commit(Ly::B_QEMPTY);
@@ -466,8 +474,9 @@ __global__ void __launch_bounds__(320, 1)
           rs = (rs4[0] + rs4[1]) + (rs4[2] + rs4[3]);
         }
         if (rescale) {
-          // O of this row scaled by alpha.  PV of the previous tile has
-          // completed: the commit that signalled this tile's S covers it.
+          // O of this row scaled by alpha before this tile's PV accumulates
+          // into it.  PV of the previous tile has completed: the commit that
+          // signalled this tile's S covers it.
 #pragma unroll
           for (int cc = 0; cc < D / 32; ++cc) {
             uint32_t o[32];
@@ -479,9 +488,12 @@ __global__ void __launch_bounds__(320, 1)
           }
         }
         l = l * alpha + rs;
+        // P (and any O rescale) is in TMEM: this thread's stores complete,
+        // then one lane per warp signals the MMA warp.
         tmem_st_wait();
         tc_fence_before();
-        mbar_arrive(bar(Ly::B_PFULL + t));
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(Ly::B_PFULL + t));
       }
       if (!ok) break;
       // ---- epilogue: O / l, LSE
@@ -510,7 +522,8 @@ __global__ void __launch_bounds__(320, 1)
         p.LSE[(static_cast<size_t>(it.b) * p.H + it.h) * p.Lq + q] =
             (m * sl2 + __log2f(l)) * 0.6931471805599453f;
       tc_fence_before();
-      mbar_arrive(bar(Ly::B_OEMPTY + t));
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(Ly::B_OEMPTY + t));
     }
   }
 
