@@ -154,16 +154,16 @@ __global__ void __launch_bounds__(512, 1)
   if (threadIdx.x == 0) {
     mbar_init(bar(Ly::B_KVFULL), 1);
     for (int s = 0; s < Ly::STAGES; ++s) {
-      mbar_init(bar(Ly::B_QFULL + s), 32);
+      mbar_init(bar(Ly::B_QFULL + s), 1);
       mbar_init(bar(Ly::B_QEMPTY + s), 1);
     }
     for (int c = 0; c < 2; ++c) {
       mbar_init(bar(Ly::B_SFULL + c), 1);
-      mbar_init(bar(Ly::B_PFULL + c), 256);
+      mbar_init(bar(Ly::B_PFULL + c), 8);  // one arrival per compute warp
     }
     mbar_init(bar(Ly::B_DQFULL), 1);
-    mbar_init(bar(Ly::B_DQEMPTY), 128);
-    mbar_init(bar(Ly::B_DQEMPTY + 1), 128);
+    mbar_init(bar(Ly::B_DQEMPTY), 4);  // one arrival per drain warp
+    mbar_init(bar(Ly::B_DQEMPTY + 1), 4);
     mbar_init(bar(Ly::B_DKVFULL), 1);
     mbar_init(bar(Ly::B_DONE), 1);
     ab->flag = 0;
@@ -214,6 +214,7 @@ __global__ void __launch_bounds__(512, 1)
         st[c] = in ? p.LSE[row0 + q] * 1.4426950408889634f : 0.f;
         st[128 + c] = in ? p.Delta[row0 + q] : 0.f;
       }
+      __syncwarp();  // every lane's LSE / Delta entries precede the arrival
       if (lane == 0) {
         mbar_arrive_expect_tx(bar(Ly::B_QFULL + stage), 2 * Ly::TILE);
         for (int c = 0; c < Ly::KCH; ++c) {
@@ -222,8 +223,6 @@ __global__ void __launch_bounds__(512, 1)
           tma_load_4d(base + Ly::DO_OFF + stage * Ly::TILE + c * Ly::CHUNK, &tmdO,
                       bar(Ly::B_QFULL + stage), c * 64, h, i * 128, it.b);
         }
-      } else {
-        mbar_arrive(bar(Ly::B_QFULL + stage));
       }
       ++issued[stage];
       if (++stage == Ly::STAGES) {
@@ -238,83 +237,101 @@ __global__ void __launch_bounds__(512, 1)
     }
   } else if (warp == 13) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      bool ok = mbar_wait(bar(Ly::B_KVFULL), 0, ab, err, 501);
+    // The whole warp runs the schedule (warp-uniform loop state and operand
+    // descriptors); one elected lane issues each MMA group and the commits.
+    auto commit = [&](int b) {
+      if (elect_one()) tc_commit(bar(b));
+      __syncwarp();
+    };
+    bool ok = mbar_wait_warp(bar(Ly::B_KVFULL), 0, ab, err, 501);
+    tc_fence_after();
+    uint32_t stage = 0, phase = 0;
+    // Descriptors of the first K step (K-major operands) or of the first 16
+    // rows (MN-major); later steps add their byte offset >> 4.
+    const uint64_t kd = sdesc_sw128(base + Ly::K_OFF, 16, 1024);
+    const uint64_t vd = sdesc_sw128(base + Ly::V_OFF, 16, 1024);
+    const uint64_t kd_mn = sdesc_sw128(base + Ly::K_OFF, Ly::CHUNK, 1024);
+    const uint64_t dsd = sdesc_sw128(base + Ly::DS_OFF, 16, 1024);
+    const uint64_t dsd_mn = sdesc_sw128(base + Ly::DS_OFF, Ly::CHUNK, 1024);
+    auto koff = [](int k) -> uint64_t { return ((k >> 2) * Ly::CHUNK + (k & 3) * 32u) >> 4; };
+    for (int n = 0; ok && n < ntiles; ++n) {
+      if (!mbar_wait_warp(bar(Ly::B_QFULL + stage), phase, ab, err, 502)) { ok = false; break; }
       tc_fence_after();
-      uint32_t stage = 0, phase = 0;
-      const uint32_t ka = base + Ly::K_OFF, va = base + Ly::V_OFF, dsa = base + Ly::DS_OFF;
-      for (int n = 0; ok && n < ntiles; ++n) {
-        if (!mbar_wait(bar(Ly::B_QFULL + stage), phase, ab, err, 502)) { ok = false; break; }
+      const uint32_t qa = base + Ly::Q_OFF + stage * Ly::TILE;
+      const uint32_t doa = base + Ly::DO_OFF + stage * Ly::TILE;
+      const uint64_t qd = sdesc_sw128(qa, 16, 1024), qd_mn = sdesc_sw128(qa, Ly::CHUNK, 1024);
+      const uint64_t dod = sdesc_sw128(doa, 16, 1024), dod_mn = sdesc_sw128(doa, Ly::CHUNK, 1024);
+      // dP^T_A = V_j dO_A^T (queries 0-63), S^T = K_j Q_i^T (all queries),
+      // dP^T_B = V_j dO_B^T (queries 64-127).  Half A's softmax starts after
+      // the first two, overlapping dP^T_B and half B's work.
+      auto issue_dp = [&](int c, uint32_t dst) {
+        if (elect_one()) {
+#pragma unroll
+          for (int k = 0; k < D / 16; ++k)
+            mma_ss(dst, vd + koff(k), dod + koff(k) + c * (8192u >> 4), IDESC_DP, k > 0 ? 1u : 0u);
+        }
+        __syncwarp();
+      };
+      issue_dp(0, tmem + Ly::TM_DPA);
+      if (D == 128 && n > 0) {  // dQ half 0 of the previous tile sits in S^T's upper half
+        if (!mbar_wait_warp(bar(Ly::B_DQEMPTY), (n - 1) & 1, ab, err, 503)) { ok = false; break; }
         tc_fence_after();
-        const uint32_t qa = base + Ly::Q_OFF + stage * Ly::TILE;
-        const uint32_t doa = base + Ly::DO_OFF + stage * Ly::TILE;
-        // dP^T_A = V_j dO_A^T (queries 0-63), S^T = K_j Q_i^T (all queries),
-        // dP^T_B = V_j dO_B^T (queries 64-127).  Half A's softmax starts after
-        // the first two, overlapping dP^T_B and half B's work.
-        auto issue_dp = [&](int c, uint32_t dst) {
+      }
+      if (elect_one()) {
 #pragma unroll
-          for (int k = 0; k < D / 16; ++k) {
-            const uint32_t off = (k >> 2) * Ly::CHUNK + (k & 3) * 32u;
-            mma_ss(dst, sdesc_sw128(va + off, 16, 1024),
-                   sdesc_sw128(doa + off + c * 8192u, 16, 1024), IDESC_DP, k > 0 ? 1u : 0u);
-          }
-        };
-        issue_dp(0, tmem + Ly::TM_DPA);
-        if (D == 128 && n > 0) {  // dQ half 0 of the previous tile sits in S^T's upper half
-          if (!mbar_wait(bar(Ly::B_DQEMPTY), (n - 1) & 1, ab, err, 503)) { ok = false; break; }
-          tc_fence_after();
-        }
+        for (int k = 0; k < D / 16; ++k)
+          mma_ss(tmem + Ly::TM_S, kd + koff(k), qd + koff(k), IDESC_S, k > 0 ? 1u : 0u);
+      }
+      __syncwarp();
+      commit(Ly::B_SFULL);
+      if (D == 128 && n > 0) {  // dQ half 1 sits in dP^T_B's columns
+        if (!mbar_wait_warp(bar(Ly::B_DQEMPTY + 1), (n - 1) & 1, ab, err, 507)) { ok = false; break; }
+        tc_fence_after();
+      }
+      issue_dp(1, tmem + Ly::TM_DPB);
+      commit(Ly::B_SFULL + 1);
+      // dV += P^T_c dO_c and dK += dS^T_c Q_c as each half's P^T / dS^T lands.
 #pragma unroll
-        for (int k = 0; k < D / 16; ++k) {
-          const uint32_t off = (k >> 2) * Ly::CHUNK + (k & 3) * 32u;
-          mma_ss(tmem + Ly::TM_S, sdesc_sw128(ka + off, 16, 1024), sdesc_sw128(qa + off, 16, 1024),
-                 IDESC_S, k > 0 ? 1u : 0u);
-        }
-        tc_commit(bar(Ly::B_SFULL));
-        if (D == 128 && n > 0) {  // dQ half 1 sits in dP^T_B's columns
-          if (!mbar_wait(bar(Ly::B_DQEMPTY + 1), (n - 1) & 1, ab, err, 507)) { ok = false; break; }
-          tc_fence_after();
-        }
-        issue_dp(1, tmem + Ly::TM_DPB);
-        tc_commit(bar(Ly::B_SFULL + 1));
-        if (!ok) break;
-        // dV += P^T_c dO_c and dK += dS^T_c Q_c as each half's P^T / dS^T lands.
-#pragma unroll
-        for (int c = 0; c < 2; ++c) {
-          if (!mbar_wait(bar(Ly::B_PFULL + c), n & 1, ab, err, 504 + c)) { ok = false; break; }
-          tc_fence_after();
+      for (int c = 0; c < 2; ++c) {
+        if (!mbar_wait_warp(bar(Ly::B_PFULL + c), n & 1, ab, err, 504 + c)) { ok = false; break; }
+        tc_fence_after();
+        if (elect_one()) {
 #pragma unroll
           for (int k = 0; k < 4; ++k)
             mma_ts(tmem + Ly::TM_DV, tmem + Ly::TM_S + 64 * c + (k >> 1) * 32u + (k & 1) * 8u,
-                   sdesc_sw128(doa + 2048u * (4 * c + k), Ly::CHUNK, 1024), IDESC_KN,
+                   dod_mn + ((2048u * (4 * c + k)) >> 4), IDESC_KN,
                    (n > 0 || c > 0 || k > 0) ? 1u : 0u);
 #pragma unroll
           for (int k = 0; k < 4; ++k)
-            mma_ss(tmem + Ly::TM_DK, sdesc_sw128(dsa + c * Ly::CHUNK + 32u * k, 16, 1024),
-                   sdesc_sw128(qa + 2048u * (4 * c + k), Ly::CHUNK, 1024), IDESC_KN,
+            mma_ss(tmem + Ly::TM_DK, dsd + ((c * Ly::CHUNK + 32u * k) >> 4),
+                   qd_mn + ((2048u * (4 * c + k)) >> 4), IDESC_KN,
                    (n > 0 || c > 0 || k > 0) ? 1u : 0u);
         }
-        if (!ok) break;
-        if (D != 128 && n > 0) {
-          if (!mbar_wait(bar(Ly::B_DQEMPTY), (n - 1) & 1, ab, err, 506)) { ok = false; break; }
-          tc_fence_after();
-        }
-        // dQ_i = dS K_j   (dS read MN-major from the dS^T tile, K_j MN-major)
+        __syncwarp();
+      }
+      if (!ok) break;
+      if (D != 128 && n > 0) {
+        if (!mbar_wait_warp(bar(Ly::B_DQEMPTY), (n - 1) & 1, ab, err, 506)) { ok = false; break; }
+        tc_fence_after();
+      }
+      // dQ_i = dS K_j   (dS read MN-major from the dS^T tile, K_j MN-major)
+      if (elect_one()) {
 #pragma unroll
         for (int k = 0; k < 8; ++k)
-          mma_ss(tmem + Ly::tm_dq(0), sdesc_sw128(dsa + 2048u * k, Ly::CHUNK, 1024),
-                 sdesc_sw128(ka + 2048u * k, Ly::CHUNK, 1024), IDESC_MN, k > 0 ? 1u : 0u);
-        tc_commit(bar(Ly::B_DQFULL));
-        tc_commit(bar(Ly::B_QEMPTY + stage));
-        if (++stage == Ly::STAGES) {
-          stage = 0;
-          phase ^= 1u;
-        }
+          mma_ss(tmem + Ly::tm_dq(0), dsd_mn + ((2048u * k) >> 4), kd_mn + ((2048u * k) >> 4),
+                 IDESC_MN, k > 0 ? 1u : 0u);
       }
-      if (ok) tc_commit(bar(Ly::B_DKVFULL));
-      tc_commit(bar(Ly::B_DONE));
-      mbar_wait_drain(bar(Ly::B_DONE), 0);
+      __syncwarp();
+      commit(Ly::B_DQFULL);
+      commit(Ly::B_QEMPTY + stage);
+      if (++stage == Ly::STAGES) {
+        stage = 0;
+        phase ^= 1u;
+      }
     }
+    if (ok) commit(Ly::B_DKVFULL);
+    commit(Ly::B_DONE);
+    mbar_wait_drain(bar(Ly::B_DONE), 0);
   } else if (warp < 8) {
     // ------------------------------------------------------------ P^T / dS^T
     // All eight warps work on query half A, then on half B: warp w owns key
@@ -384,7 +401,8 @@ __global__ void __launch_bounds__(512, 1)
         tmem_st_wait();
         fence_proxy_async_smem();
         tc_fence_before();
-        mbar_arrive(bar(Ly::B_PFULL + hc));
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(Ly::B_PFULL + hc));
       }
       if (++stage == Ly::STAGES) stage = 0;
     }
@@ -437,7 +455,8 @@ __global__ void __launch_bounds__(512, 1)
         tmem_ld_wait32(g + 32);
         // This half is in registers: release its columns before the atomics.
         tc_fence_before();
-        mbar_arrive(bar(Ly::B_DQEMPTY + hq));
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(Ly::B_DQEMPTY + hq));
         if (q < p.Lq) {
 #pragma unroll
           for (int c4 = 0; c4 < 16; ++c4)
