@@ -203,7 +203,7 @@ __global__ void __launch_bounds__(512, 1)
       int h, i;
       bwd_tile(it, p, n, h, i);
       if (!mbar_wait_warp(bar(Ly::B_QEMPTY + stage), phase ^ 1u, ab, err, 401)) { ok = false; break; }
-      // LSE (pre-multiplied by log2 e) and Delta of the 128 query rows of tile i.
+      // -LSE (pre-multiplied by log2 e) and -Delta of the 128 query rows of tile i.
       float* st = stats + stage * 256;
       const size_t row0 = (static_cast<size_t>(it.b) * p.H + h) * p.Lq;
 #pragma unroll
@@ -211,8 +211,8 @@ __global__ void __launch_bounds__(512, 1)
         const int c = lane + 32 * u;
         const int q = i * 128 + c;
         const bool in = q < p.Lq;
-        st[c] = in ? p.LSE[row0 + q] * 1.4426950408889634f : 0.f;
-        st[128 + c] = in ? p.Delta[row0 + q] : 0.f;
+        st[c] = in ? -p.LSE[row0 + q] * 1.4426950408889634f : 0.f;
+        st[128 + c] = in ? -p.Delta[row0 + q] : 0.f;
       }
       __syncwarp();  // every lane's LSE / Delta entries precede the arrival
       if (lane == 0) {
@@ -264,15 +264,17 @@ __global__ void __launch_bounds__(512, 1)
       // dP^T_A = V_j dO_A^T (queries 0-63), S^T = K_j Q_i^T (all queries),
       // dP^T_B = V_j dO_B^T (queries 64-127).  Half A's softmax starts after
       // the first two, overlapping dP^T_B and half B's work.
-      auto issue_dp = [&](int c, uint32_t dst) {
+      // (commit_bar < 0: no commit after the group)
+      auto issue_dp = [&](int c, uint32_t dst, int commit_bar) {
         if (elect_one()) {
 #pragma unroll
           for (int k = 0; k < D / 16; ++k)
             mma_ss(dst, vd + koff(k), dod + koff(k) + c * (8192u >> 4), IDESC_DP, k > 0 ? 1u : 0u);
+          if (commit_bar >= 0) tc_commit(bar(commit_bar));
         }
         __syncwarp();
       };
-      issue_dp(0, tmem + Ly::TM_DPA);
+      issue_dp(0, tmem + Ly::TM_DPA, -1);
       if (D == 128 && n > 0) {  // dQ half 0 of the previous tile sits in S^T's upper half
         if (!mbar_wait_warp(bar(Ly::B_DQEMPTY), (n - 1) & 1, ab, err, 503)) { ok = false; break; }
         tc_fence_after();
@@ -281,15 +283,14 @@ __global__ void __launch_bounds__(512, 1)
 #pragma unroll
         for (int k = 0; k < D / 16; ++k)
           mma_ss(tmem + Ly::TM_S, kd + koff(k), qd + koff(k), IDESC_S, k > 0 ? 1u : 0u);
+        tc_commit(bar(Ly::B_SFULL));
       }
       __syncwarp();
-      commit(Ly::B_SFULL);
       if (D == 128 && n > 0) {  // dQ half 1 sits in dP^T_B's columns
         if (!mbar_wait_warp(bar(Ly::B_DQEMPTY + 1), (n - 1) & 1, ab, err, 507)) { ok = false; break; }
         tc_fence_after();
       }
-      issue_dp(1, tmem + Ly::TM_DPB);
-      commit(Ly::B_SFULL + 1);
+      issue_dp(1, tmem + Ly::TM_DPB, Ly::B_SFULL + 1);
       // dV += P^T_c dO_c and dK += dS^T_c Q_c as each half's P^T / dS^T lands.
 #pragma unroll
       for (int c = 0; c < 2; ++c) {
@@ -320,10 +321,10 @@ __global__ void __launch_bounds__(512, 1)
         for (int k = 0; k < 8; ++k)
           mma_ss(tmem + Ly::tm_dq(0), dsd_mn + ((2048u * k) >> 4), kd_mn + ((2048u * k) >> 4),
                  IDESC_MN, k > 0 ? 1u : 0u);
+        tc_commit(bar(Ly::B_DQFULL));
+        tc_commit(bar(Ly::B_QEMPTY + stage));
       }
       __syncwarp();
-      commit(Ly::B_DQFULL);
-      commit(Ly::B_QEMPTY + stage);
       if (++stage == Ly::STAGES) {
         stage = 0;
         phase ^= 1u;
@@ -367,26 +368,36 @@ __global__ void __launch_bounds__(512, 1)
         tmem_ld_wait32(sv);
         tmem_ld_wait32(dp);
         uint32_t pk[16], dk[16];
-        const float4* st4 = reinterpret_cast<const float4*>(st);
-        const float4* dl4 = reinterpret_cast<const float4*>(st + 128);
+        // Two queries per paired fp32 instruction: exponent argument
+        // S^T*c - LSE*log2e, then dS^T = P^T (dP^T - Delta).
+        const uint4* nl4 = reinterpret_cast<const uint4*>(st);        // -LSE*log2e
+        const uint4* nd4 = reinterpret_cast<const uint4*>(st + 128);  // -Delta
+        const uint64_t sl2x2 = f2_pack(sl2, sl2);
 #pragma unroll
         for (int u4 = 0; u4 < 8; ++u4) {
-          const float4 l4 = st4[u4], d4 = dl4[u4];
-          const float lse[4] = {l4.x, l4.y, l4.z, l4.w};
-          const float dlt[4] = {d4.x, d4.y, d4.z, d4.w};
-          float pv[4], dv[4];
+          const uint4 l4 = nl4[u4], d4 = nd4[u4];
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int cl = 4 * u4 + e;
-            float pp = ex2(fmaf(__uint_as_float(sv[cl]), sl2, -lse[e]));
-            if (!full) pp = (cl >= lo && cl < hi) ? pp : 0.f;
-            pv[e] = pp;
-            dv[e] = pp * (__uint_as_float(dp[cl]) - dlt[e]);
+          for (int e = 0; e < 2; ++e) {
+            const int cl = 4 * u4 + 2 * e;
+            const uint64_t nl = e ? f2_pack(__uint_as_float(l4.z), __uint_as_float(l4.w))
+                                  : f2_pack(__uint_as_float(l4.x), __uint_as_float(l4.y));
+            const uint64_t nd = e ? f2_pack(__uint_as_float(d4.z), __uint_as_float(d4.w))
+                                  : f2_pack(__uint_as_float(d4.x), __uint_as_float(d4.y));
+            float a0, a1;
+            f2_unpack(ffma2(f2_pack(__uint_as_float(sv[cl]), __uint_as_float(sv[cl + 1])), sl2x2, nl),
+                      a0, a1);
+            float p0 = ex2(a0), p1 = ex2(a1);
+            if (!full) {
+              p0 = (cl >= lo && cl < hi) ? p0 : 0.f;
+              p1 = (cl + 1 >= lo && cl + 1 < hi) ? p1 : 0.f;
+            }
+            const uint64_t pp = f2_pack(p0, p1);
+            float d0, d1;
+            f2_unpack(fmul2(pp, fadd2(f2_pack(__uint_as_float(dp[cl]), __uint_as_float(dp[cl + 1])), nd)),
+                      d0, d1);
+            pk[cl >> 1] = pack2<T>(p0, p1);
+            dk[cl >> 1] = pack2<T>(d0, d1);
           }
-          pk[2 * u4] = pack2<T>(pv[0], pv[1]);
-          pk[2 * u4 + 1] = pack2<T>(pv[2], pv[3]);
-          dk[2 * u4] = pack2<T>(dv[0], dv[1]);
-          dk[2 * u4 + 1] = pack2<T>(dv[2], dv[3]);
         }
         // P^T (16-bit pairs) over the first 16 of this chunk's own S^T columns.
         tmem_st16(tS, pk);
