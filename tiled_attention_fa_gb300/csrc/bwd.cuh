@@ -471,9 +471,9 @@ __global__ void __launch_bounds__(512, 1)
         if (q < p.Lq) {
 #pragma unroll
           for (int c4 = 0; c4 < 16; ++c4)
-            atomicAdd(acc + static_cast<size_t>(16 * hq + c4) * p.Lpad,
-                      make_float4(__uint_as_float(g[4 * c4]), __uint_as_float(g[4 * c4 + 1]),
-                                  __uint_as_float(g[4 * c4 + 2]), __uint_as_float(g[4 * c4 + 3])));
+            red_add_v4(reinterpret_cast<float*>(acc + static_cast<size_t>(16 * hq + c4) * p.Lpad),
+                       __uint_as_float(g[4 * c4]), __uint_as_float(g[4 * c4 + 1]),
+                       __uint_as_float(g[4 * c4 + 2]), __uint_as_float(g[4 * c4 + 3]));
         }
       }
     }

@@ -389,6 +389,14 @@ __device__ __forceinline__ void tmem_st_wait() {
 
 // ------------------------------------------------------------------ misc
 
+// Fire-and-forget fp32 reduction of four consecutive floats into global memory.
+__device__ __forceinline__ void red_add_v4(float* addr, float a, float b, float c, float d) {
+  asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(addr), "f"(a), "f"(b),
+               "f"(c), "f"(d)
+               : "memory");
+}
+
+
 __device__ __forceinline__ float ex2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
