@@ -471,13 +471,17 @@ __global__ void __launch_bounds__(512, 1)
         if (q < p.Lq) {
 #pragma unroll
           for (int c4 = 0; c4 < 16; ++c4) {
-            // Pace the reductions: issued back to back they compete with the
-            // compute warps' shared-memory and TMEM traffic of the next tile
-            // (measured: 5.53 -> 5.24 ms at B8 H32 L4096 D128 with a ~200 ns
-            // pause before every fourth; pauses of 400 ns let the drain fall
-            // behind the tile rate).  A late drain only delays the MMA warp's
+            // Pace the second half's reductions (D = 128 only): issued back
+            // to back they overlap the first query half of the next tile and
+            // slow its compute warps.  Measured at B8 H32 L4096 D128: 5.54 ms
+            // unpaced, 5.15 ms with four 512 ns pauses, which is 0.7 of the
+            // ~2.9 us a 128 x 128 tile takes at 2.07 GHz (lower clocks only
+            // lengthen the tile).  __nanosleep(t) sleeps for the power of two
+            // above t (300-500 -> 512 ns); four pauses of 1,024 ns outlast a
+            // tile and the drain falls behind (7.4 ms); pausing the first half
+            // instead is slower.  A late drain only delays the MMA warp's
             // bounded wait on the dQ-empty barrier.
-            if ((c4 & 3) == 3) __nanosleep(200);
+            if (hq == 1 && (c4 & 3) == 3) __nanosleep(384);
             red_add_v4(reinterpret_cast<float*>(acc + static_cast<size_t>(16 * hq + c4) * p.Lpad),
                        __uint_as_float(g[4 * c4]), __uint_as_float(g[4 * c4 + 1]),
                        __uint_as_float(g[4 * c4 + 2]), __uint_as_float(g[4 * c4 + 3]));
