@@ -58,6 +58,7 @@ struct BwdParams {
   int n_q;      // ceil(Lq / 128) Q tiles
   int Lpad;     // n_q * 128
   int n_items;  // B * Hkv * n_kv
+  int n_pairs;  // B * Hkv * ceil(n_kv / 2): work units of the persistent CTAs
   float sl2;    // log2(e) / sqrt(D)
   float scale;  // 1 / sqrt(D)
 };
@@ -72,7 +73,8 @@ struct BwdLayout {
   // then the 1024-byte aligned operand tiles.
   static constexpr int B_KVFULL = 0, B_QFULL = 1, B_QEMPTY = 1 + STAGES, B_SFULL = 1 + 2 * STAGES,
                        B_PFULL = B_SFULL + 2, B_DQFULL = B_PFULL + 2, B_DQEMPTY = B_DQFULL + 1,
-                       B_DKVFULL = B_DQEMPTY + 2, B_DONE = B_DKVFULL + 1, NBAR = B_DONE + 1;
+                       B_DKVFULL = B_DQEMPTY + 2, B_DONE = B_DKVFULL + 1, B_KVEMPTY = B_DONE + 1,
+                       NBAR = B_KVEMPTY + 1;
   static constexpr uint32_t BAR_OFF = 0;
   static constexpr uint32_t MISC_OFF = BAR_OFF + NBAR * 8;              // tmem slot, abort flag
   static constexpr uint32_t STAT_OFF = (MISC_OFF + 16 + 15) / 16 * 16;  // [STAGES][2][128] f32
@@ -115,6 +117,21 @@ __device__ __forceinline__ BwdItem bwd_decode(int item, const BwdParams& p) {
   return it;
 }
 
+// Work unit u of the persistent CTAs: K/V tiles j and n_kv-1-j of one
+// (batch, K/V head), the longer first.  Under causal masking tile j visits
+// n_q - j Q tiles (Lq = Lk), so a pair's work is the same for every j; the
+// pairs of one head are consecutive, so the CTAs running at the same time
+// share a few heads' Q / dO in L2.  Returns false for the missing second tile
+// of the middle pair when n_kv is odd.
+__device__ __forceinline__ bool bwd_pair_item(int u, int s, const BwdParams& p, int& item) {
+  const int per = (p.n_kv + 1) / 2;
+  const int bh = u / per, jp = u - bh * per;
+  const int j = s ? p.n_kv - 1 - jp : jp;
+  if (s && j == jp) return false;
+  item = bh * p.n_kv + j;
+  return true;
+}
+
 // n-th (head, Q tile) pair of an item: heads of the group outer, tiles inner.
 __device__ __forceinline__ void bwd_tile(const BwdItem& it, const BwdParams& p, int n, int& h,
                                          int& i) {
@@ -150,9 +167,9 @@ __global__ void __launch_bounds__(512, 1)
     if (threadIdx.x == 0) atomicCAS(err, 0u, 499u);
     return;
   }
-  const BwdItem it = bwd_decode(blockIdx.x, p);
   if (threadIdx.x == 0) {
     mbar_init(bar(Ly::B_KVFULL), 1);
+    mbar_init(bar(Ly::B_KVEMPTY), 1);
     for (int s = 0; s < Ly::STAGES; ++s) {
       mbar_init(bar(Ly::B_QFULL + s), 1);
       mbar_init(bar(Ly::B_QEMPTY + s), 1);
@@ -183,12 +200,28 @@ __global__ void __launch_bounds__(512, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const int ntiles = it.ntiles;
+  // Persistent CTAs: work units (pairs of K/V tiles, bwd_pair_item)
+  // blockIdx.x, blockIdx.x + gridDim.x, ...  Every
+  // per-tile barrier phase runs on the CTA's tile counter g, so one item's
+  // last tiles (dQ drain, dK/dV epilogue) overlap the next item's first ones;
+  // K_j / V_j of the next item load once the last MMA reading the current ones
+  // completes (K/V-empty barrier).
+  const int G = static_cast<int>(gridDim.x);
 
   if (warp == 12) {
     // ------------------------------------------------------------ producer (whole warp)
     bool ok = true;
     uint32_t issued[Ly::STAGES] = {0, 0};
+    uint32_t stage = 0, phase = 0, kv_cnt = 0;
+    for (int u = 2 * static_cast<int>(blockIdx.x); ok && u < 2 * p.n_pairs;
+         u += (u & 1) ? 2 * G - 1 : 1) {
+    int item;
+    if (!bwd_pair_item(u >> 1, u & 1, p, item)) continue;
+    const BwdItem it = bwd_decode(item, p);
+    if (kv_cnt > 0 && !mbar_wait_warp(bar(Ly::B_KVEMPTY), (kv_cnt - 1) & 1, ab, err, 402)) {
+      ok = false;
+      break;
+    }
     if (lane == 0) {
       mbar_arrive_expect_tx(bar(Ly::B_KVFULL), 2 * Ly::TILE);
       for (int c = 0; c < Ly::KCH; ++c) {
@@ -198,8 +231,8 @@ __global__ void __launch_bounds__(512, 1)
                     it.j * 128, it.b);
       }
     }
-    uint32_t stage = 0, phase = 0;
-    for (int n = 0; n < ntiles; ++n) {
+    ++kv_cnt;
+    for (int n = 0; n < it.ntiles; ++n) {
       int h, i;
       bwd_tile(it, p, n, h, i);
       if (!mbar_wait_warp(bar(Ly::B_QEMPTY + stage), phase ^ 1u, ab, err, 401)) { ok = false; break; }
@@ -230,8 +263,9 @@ __global__ void __launch_bounds__(512, 1)
         phase ^= 1u;
       }
     }
+    }
     if (!ok && lane == 0) {
-      mbar_wait_drain(bar(Ly::B_KVFULL), 0);
+      if (kv_cnt > 0) mbar_wait_drain(bar(Ly::B_KVFULL), (kv_cnt - 1) & 1);
       for (int s = 0; s < Ly::STAGES; ++s)
         if (issued[s] > 0) mbar_wait_drain(bar(Ly::B_QFULL + s), (issued[s] - 1) & 1);
     }
@@ -243,9 +277,8 @@ __global__ void __launch_bounds__(512, 1)
       if (elect_one()) tc_commit(bar(b));
       __syncwarp();
     };
-    bool ok = mbar_wait_warp(bar(Ly::B_KVFULL), 0, ab, err, 501);
-    tc_fence_after();
-    uint32_t stage = 0, phase = 0;
+    bool ok = true;
+    uint32_t stage = 0, phase = 0, g = 0, kv_cnt = 0;
     // Descriptors of the first K step (K-major operands) or of the first 16
     // rows (MN-major); later steps add their byte offset >> 4.
     const uint64_t kd = sdesc_sw128(base + Ly::K_OFF, 16, 1024);
@@ -254,7 +287,15 @@ __global__ void __launch_bounds__(512, 1)
     const uint64_t dsd = sdesc_sw128(base + Ly::DS_OFF, 16, 1024);
     const uint64_t dsd_mn = sdesc_sw128(base + Ly::DS_OFF, Ly::CHUNK, 1024);
     auto koff = [](int k) -> uint64_t { return ((k >> 2) * Ly::CHUNK + (k & 3) * 32u) >> 4; };
-    for (int n = 0; ok && n < ntiles; ++n) {
+    for (int u = 2 * static_cast<int>(blockIdx.x); ok && u < 2 * p.n_pairs;
+         u += (u & 1) ? 2 * G - 1 : 1) {
+    int item;
+    if (!bwd_pair_item(u >> 1, u & 1, p, item)) continue;
+    const BwdItem it = bwd_decode(item, p);
+    if (!mbar_wait_warp(bar(Ly::B_KVFULL), kv_cnt & 1, ab, err, 501)) { ok = false; break; }
+    tc_fence_after();
+    // n: tile within the item (accumulate flags); g: tile of the CTA (phases)
+    for (int n = 0; ok && n < it.ntiles; ++n, ++g) {
       if (!mbar_wait_warp(bar(Ly::B_QFULL + stage), phase, ab, err, 502)) { ok = false; break; }
       tc_fence_after();
       const uint32_t qa = base + Ly::Q_OFF + stage * Ly::TILE;
@@ -275,8 +316,8 @@ __global__ void __launch_bounds__(512, 1)
         __syncwarp();
       };
       issue_dp(0, tmem + Ly::TM_DPA, -1);
-      if (D == 128 && n > 0) {  // dQ half 0 of the previous tile sits in S^T's upper half
-        if (!mbar_wait_warp(bar(Ly::B_DQEMPTY), (n - 1) & 1, ab, err, 503)) { ok = false; break; }
+      if (D == 128 && g > 0) {  // dQ half 0 of the previous tile sits in S^T's upper half
+        if (!mbar_wait_warp(bar(Ly::B_DQEMPTY), (g - 1) & 1, ab, err, 503)) { ok = false; break; }
         tc_fence_after();
       }
       if (elect_one()) {
@@ -286,15 +327,15 @@ __global__ void __launch_bounds__(512, 1)
         tc_commit(bar(Ly::B_SFULL));
       }
       __syncwarp();
-      if (D == 128 && n > 0) {  // dQ half 1 sits in dP^T_B's columns
-        if (!mbar_wait_warp(bar(Ly::B_DQEMPTY + 1), (n - 1) & 1, ab, err, 507)) { ok = false; break; }
+      if (D == 128 && g > 0) {  // dQ half 1 sits in dP^T_B's columns
+        if (!mbar_wait_warp(bar(Ly::B_DQEMPTY + 1), (g - 1) & 1, ab, err, 507)) { ok = false; break; }
         tc_fence_after();
       }
       issue_dp(1, tmem + Ly::TM_DPB, Ly::B_SFULL + 1);
       // dV += P^T_c dO_c and dK += dS^T_c Q_c as each half's P^T / dS^T lands.
 #pragma unroll
       for (int c = 0; c < 2; ++c) {
-        if (!mbar_wait_warp(bar(Ly::B_PFULL + c), n & 1, ab, err, 504 + c)) { ok = false; break; }
+        if (!mbar_wait_warp(bar(Ly::B_PFULL + c), g & 1, ab, err, 504 + c)) { ok = false; break; }
         tc_fence_after();
         if (elect_one()) {
 #pragma unroll
@@ -311,8 +352,8 @@ __global__ void __launch_bounds__(512, 1)
         __syncwarp();
       }
       if (!ok) break;
-      if (D != 128 && n > 0) {
-        if (!mbar_wait_warp(bar(Ly::B_DQEMPTY), (n - 1) & 1, ab, err, 506)) { ok = false; break; }
+      if (D != 128 && g > 0) {
+        if (!mbar_wait_warp(bar(Ly::B_DQEMPTY), (g - 1) & 1, ab, err, 506)) { ok = false; break; }
         tc_fence_after();
       }
       // dQ_i = dS K_j   (dS read MN-major from the dS^T tile, K_j MN-major)
@@ -330,7 +371,15 @@ __global__ void __launch_bounds__(512, 1)
         phase ^= 1u;
       }
     }
-    if (ok) commit(Ly::B_DKVFULL);
+    if (!ok) break;
+    // dK / dV of this item are final; K_j / V_j are no longer read.
+    if (elect_one()) {
+      tc_commit(bar(Ly::B_DKVFULL));
+      tc_commit(bar(Ly::B_KVEMPTY));
+    }
+    __syncwarp();
+    ++kv_cnt;
+    }
     commit(Ly::B_DONE);
     mbar_wait_drain(bar(Ly::B_DONE), 0);
   } else if (warp < 8) {
@@ -340,17 +389,22 @@ __global__ void __launch_bounds__(512, 1)
     // current half.
     const int sub = warp >> 2;        // 32-query chunk within a half
     const int r = threadIdx.x & 127;  // key row within the tile == TMEM lane
-    const int kr = it.j * 128 + r;
     const uint32_t lane_off = ((warp & 3u) * 32u) << 16;
     const float sl2 = p.sl2;
     bool ok = true;
-    uint32_t stage = 0;
-    for (int n = 0; ok && n < ntiles; ++n) {
+    uint32_t stage = 0, g = 0, kv_cnt = 0;
+    for (int u = 2 * static_cast<int>(blockIdx.x); ok && u < 2 * p.n_pairs;
+         u += (u & 1) ? 2 * G - 1 : 1) {
+    int item;
+    if (!bwd_pair_item(u >> 1, u & 1, p, item)) continue;
+    const BwdItem it = bwd_decode(item, p);
+    const int kr = it.j * 128 + r;
+    for (int n = 0; ok && n < it.ntiles; ++n, ++g) {
       int h, i;
       bwd_tile(it, p, n, h, i);
 #pragma unroll
       for (int hc = 0; hc < 2; ++hc) {
-        if (!mbar_wait_warp(bar(Ly::B_SFULL + hc), n & 1, ab, err, 601)) { ok = false; break; }
+        if (!mbar_wait_warp(bar(Ly::B_SFULL + hc), g & 1, ab, err, 601)) { ok = false; break; }
         tc_fence_after();
         const int cbase = 64 * hc + 32 * sub;  // first query column of this chunk
         const uint32_t tS = tmem + lane_off + Ly::TM_S + cbase;
@@ -419,7 +473,9 @@ __global__ void __launch_bounds__(512, 1)
     }
     const int hc = sub;  // epilogue role: warps 0-3 write dK, warps 4-7 write dV
     // Epilogue: warpgroup A writes dK (scaled by 1/sqrt(D)), B writes dV.
-    if (ok && mbar_wait_warp(bar(Ly::B_DKVFULL), 0, ab, err, 602)) {
+    if (!ok) break;
+    if (!mbar_wait_warp(bar(Ly::B_DKVFULL), kv_cnt & 1, ab, err, 602)) { ok = false; break; }
+    {
       tc_fence_after();
       void* dst_base = hc == 0 ? p.dK : p.dV;
       const float sc = hc == 0 ? p.scale : 1.f;
@@ -443,14 +499,23 @@ __global__ void __launch_bounds__(512, 1)
         }
       }
     }
+    ++kv_cnt;
+    }
   } else if (warp < 12) {
     // ------------------------------------------------------------ dQ drain
     const int r = threadIdx.x & 127;  // query row within the Q tile == TMEM lane
     const uint32_t lane_off = ((warp & 3u) * 32u) << 16;
-    for (int n = 0; n < ntiles; ++n) {
+    bool ok = true;
+    uint32_t g = 0;
+    for (int u = 2 * static_cast<int>(blockIdx.x); ok && u < 2 * p.n_pairs;
+         u += (u & 1) ? 2 * G - 1 : 1) {
+    int item;
+    if (!bwd_pair_item(u >> 1, u & 1, p, item)) continue;
+    const BwdItem it = bwd_decode(item, p);
+    for (int n = 0; n < it.ntiles; ++n, ++g) {
       int h, i;
       bwd_tile(it, p, n, h, i);
-      if (!mbar_wait_warp(bar(Ly::B_DQFULL), n & 1, ab, err, 701)) break;
+      if (!mbar_wait_warp(bar(Ly::B_DQFULL), g & 1, ab, err, 701)) { ok = false; break; }
       tc_fence_after();
       const int q = i * 128 + r;
       // accumulator layout [B, H, D/4, Lpad, 4]: a warp's 32 rows of one
@@ -459,11 +524,11 @@ __global__ void __launch_bounds__(512, 1)
                     (static_cast<size_t>(it.b) * p.H + h) * (D / 4) * p.Lpad + q;
 #pragma unroll
       for (int hq = 0; hq < Ly::NDQ; ++hq) {
-        uint32_t g[64];
-        tmem_ld32(tmem + lane_off + Ly::tm_dq(hq), g);
-        tmem_ld32(tmem + lane_off + Ly::tm_dq(hq) + 32, g + 32);
-        tmem_ld_wait32(g);
-        tmem_ld_wait32(g + 32);
+        uint32_t gq[64];
+        tmem_ld32(tmem + lane_off + Ly::tm_dq(hq), gq);
+        tmem_ld32(tmem + lane_off + Ly::tm_dq(hq) + 32, gq + 32);
+        tmem_ld_wait32(gq);
+        tmem_ld_wait32(gq + 32);
         // This half is in registers: release its columns before the atomics.
         tc_fence_before();
         __syncwarp();
@@ -483,11 +548,12 @@ __global__ void __launch_bounds__(512, 1)
             // bounded wait on the dQ-empty barrier.
             if (hq == 1 && (c4 & 3) == 3) __nanosleep(384);
             red_add_v4(reinterpret_cast<float*>(acc + static_cast<size_t>(16 * hq + c4) * p.Lpad),
-                       __uint_as_float(g[4 * c4]), __uint_as_float(g[4 * c4 + 1]),
-                       __uint_as_float(g[4 * c4 + 2]), __uint_as_float(g[4 * c4 + 3]));
+                       __uint_as_float(gq[4 * c4]), __uint_as_float(gq[4 * c4 + 1]),
+                       __uint_as_float(gq[4 * c4 + 2]), __uint_as_float(gq[4 * c4 + 3]));
           }
         }
       }
+    }
     }
   }
 
