@@ -10,8 +10,8 @@
 //      accumulator with atomics laid out to match the accumulator fragments;
 //   3. post-process: scale and convert the dQ accumulator back to BSHD.
 //
-// GB300 design of the main pass (512 threads, one CTA per SM, one K/V tile
-// of 128 keys per CTA):
+// GB300 design of the main pass (512 threads, one persistent CTA per SM; a
+// work unit is a pair of 128-key K/V tiles of one head, see bwd_pair_item):
 //   warps 0-7  compute warps: each query half of a tile (columns 0-63, then
 //              64-127) is split over all eight, warp w taking 32 columns
 //              of key rows 32*(w%4).. (its TMEM lanes); a thread owns one
@@ -23,9 +23,9 @@
 //              warps 4-7 dV.
 //   warps 8-11 dQ drain: thread r owns query row r; reads the dQ tile from
 //              TMEM and adds it into the fp32 accumulator with 16-byte
-//              vector atomics.
-//   warp  12   TMA producer: K_j, V_j once; then Q_i, dO_i (and LSE_i,
-//              Delta_i) through a two-slot ring.
+//              vector reductions (the second half's paced).
+//   warp  12   TMA producer: K_j, V_j once per K/V tile; then Q_i, dO_i (and
+//              LSE_i, Delta_i) through a two-slot ring.
 //   warp  13   TMEM allocator and the single tcgen05.mma issuing thread.
 //   warps 14-15 idle.
 // Per tile the MMA thread issues dP^T for query half A, S^T for all 128
