@@ -9,6 +9,7 @@ package only marshals torch tensors into it.  Build the library with
 from .api import (  # noqa: F401
     DecodeHostRunner,
     Fp8HostRunner,
+    HostPipeline,
     HostRunner,
     alloc_workspace,
     attention_backward,
@@ -28,5 +29,5 @@ from .api import (  # noqa: F401
 )
 
 __all__ = ["fwd", "bwd_preprocess", "bwd", "attention_backward", "bwd_main", "bwd_postprocess", "workspace_size",
-           "alloc_workspace", "check_device_error", "HostRunner", "decode", "decode_workspace_size",
+           "alloc_workspace", "check_device_error", "HostRunner", "HostPipeline", "decode", "decode_workspace_size",
            "decode_slices", "decode_merge", "alloc_decode_workspace", "DecodeHostRunner", "fwd_fp8", "Fp8HostRunner"]

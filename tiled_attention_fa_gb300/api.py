@@ -4,7 +4,9 @@ Every function takes torch CUDA tensors (PyTorch supplies device memory and
 the current stream), checks layout and dtype, and calls the matching C entry
 point.  All arithmetic runs in the library's CUDA kernels; there is no CPU or
 framework fallback.  ``HostRunner`` serves callers whose data lives on the
-host: it copies through pinned host memory around the same calls.
+host: it copies through pinned host memory around the same calls;
+``HostPipeline`` does the same for a sequence of batches with the copies of
+one batch overlapping the kernels of its neighbours.
 """
 
 from __future__ import annotations
@@ -347,6 +349,91 @@ class HostRunner:
                           ("dv", self.dv)):
             self.h_out[name].copy_(src, non_blocking=True)
         return self.h_out
+
+
+class HostPipeline:
+    """Forward + backward over a stream of host-resident batches, with each
+    batch's copies overlapping its neighbours' kernels.
+
+    ``submit(q, k, v, do)`` enqueues one step (pinned host inputs) and returns
+    the pinned host tensors its O, LSE, dQ, dK, dV will land in; ``wait()``
+    blocks until every submitted step is done.  ``depth`` sets of device
+    buffers rotate: step s uploads into set s % depth on an upload stream, runs
+    the forward, preprocess and backward on the compute stream once its inputs
+    are in and the set's previous outputs have been read back, and reads its
+    results back on a download stream.  A step's host outputs are valid after
+    ``wait()`` (or once the step ``depth`` later has been submitted and has
+    started its download) and are reused by step s + depth.
+    """
+
+    def __init__(self, B, L, H, Hkv, D, dtype=torch.float16, causal=False, device="cuda",
+                 Lk=None, depth=2):
+        self.causal = causal
+        self.depth = depth
+        dev = torch.device(device)
+        Lk = L if Lk is None else Lk
+        self.sets = []
+        pin = dict(pin_memory=True)
+        for _ in range(depth):
+            d = {"q": torch.empty(B, L, H, D, dtype=dtype, device=dev),
+                 "k": torch.empty(B, Lk, Hkv, D, dtype=dtype, device=dev)}
+            d["v"] = torch.empty_like(d["k"])
+            d["do"] = torch.empty_like(d["q"])
+            d["o"] = torch.empty_like(d["q"])
+            d["lse"] = torch.empty(B, H, L, dtype=torch.float32, device=dev)
+            d["delta"] = torch.empty_like(d["lse"])
+            d["dq"] = torch.empty_like(d["q"])
+            d["dk"] = torch.empty_like(d["k"])
+            d["dv"] = torch.empty_like(d["k"])
+            d["acc"] = alloc_workspace(B, L, H, D, dev)
+            d["h_out"] = {n: torch.empty(d[n].shape, dtype=d[n].dtype, **pin)
+                          for n in ("o", "lse", "dq", "dk", "dv")}
+            d["in_ready"] = torch.cuda.Event()
+            d["computed"] = torch.cuda.Event()
+            d["read_back"] = torch.cuda.Event()
+            d["used"] = False
+            self.sets.append(d)
+        self.up = torch.cuda.Stream(device=dev)
+        self.compute = torch.cuda.Stream(device=dev)
+        self.down = torch.cuda.Stream(device=dev)
+        self.n = 0
+
+    def h2d_bytes(self) -> int:
+        d = self.sets[0]
+        return sum(d[n].numel() * d[n].element_size() for n in ("q", "k", "v", "do"))
+
+    def d2h_bytes(self) -> int:
+        return sum(t.numel() * t.element_size() for t in self.sets[0]["h_out"].values())
+
+    def submit(self, q, k, v, do):
+        d = self.sets[self.n % self.depth]
+        self.n += 1
+        if d["used"]:
+            self.up.wait_event(d["computed"])  # the set's previous step has read its inputs
+        with torch.cuda.stream(self.up):
+            for name, src in (("q", q), ("k", k), ("v", v), ("do", do)):
+                d[name].copy_(src, non_blocking=True)
+            d["in_ready"].record(self.up)
+        self.compute.wait_event(d["in_ready"])
+        if d["used"]:
+            self.compute.wait_event(d["read_back"])  # its previous outputs are on the host
+        fwd(d["q"], d["k"], d["v"], self.causal, out=d["o"], lse=d["lse"], stream=self.compute)
+        bwd_preprocess(d["o"], d["do"], delta=d["delta"], dq_accum=d["acc"], stream=self.compute)
+        bwd(d["q"], d["k"], d["v"], d["o"], d["do"], d["lse"], d["delta"], self.causal,
+            dq=d["dq"], dk=d["dk"], dv=d["dv"], dq_accum=d["acc"], accum_zeroed=True,
+            stream=self.compute)
+        d["computed"].record(self.compute)
+        self.down.wait_event(d["computed"])
+        with torch.cuda.stream(self.down):
+            for name, dst in d["h_out"].items():
+                dst.copy_(d[name], non_blocking=True)
+            d["read_back"].record(self.down)
+        d["used"] = True
+        return d["h_out"]
+
+    def wait(self):
+        for st in (self.up, self.compute, self.down):
+            st.synchronize()
 
 
 class DecodeHostRunner:
