@@ -66,7 +66,8 @@ static fa_status launch_bwd(const void* Q, const void* K, const void* V, const v
   p.n_q = Lpad / 128;
   p.Lpad = Lpad;
   p.n_items = B * Hkv * p.n_kv;
-  p.n_pairs = B * Hkv * ((p.n_kv + 1) / 2);
+  p.ipu = p.causal ? 2 : 1;
+  p.n_units = p.causal ? B * Hkv * ((p.n_kv + 1) / 2) : p.n_items;
   p.scale = 1.f / sqrtf(static_cast<float>(D));
   p.sl2 = 1.4426950408889634f * p.scale;
   int dev = 0, optin = 0;
@@ -77,7 +78,7 @@ static fa_status launch_bwd(const void* Q, const void* K, const void* V, const v
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Ly::SMEM_ALLOC) !=
       cudaSuccess)
     return FA_ERR_CUDA;
-  const int grid = p.n_pairs < sm_count() ? p.n_pairs : sm_count();  // persistent CTAs
+  const int grid = p.n_units < sm_count() ? p.n_units : sm_count();  // persistent CTAs
   kern<<<grid, Ly::NTHREADS, Ly::SMEM_ALLOC, s>>>(tq, tk, tv, tdo, p);
   return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }

@@ -11,7 +11,7 @@
 //   3. post-process: scale and convert the dQ accumulator back to BSHD.
 //
 // GB300 design of the main pass (512 threads, one persistent CTA per SM; a
-// work unit is a pair of 128-key K/V tiles of one head, see bwd_pair_item):
+// work unit is one or two 128-key K/V tiles of one head, see bwd_unit_item):
 //   warps 0-7  compute warps: each query half of a tile (columns 0-63, then
 //              64-127) is split over all eight, warp w taking 32 columns
 //              of key rows 32*(w%4).. (its TMEM lanes); a thread owns one
@@ -58,7 +58,8 @@ struct BwdParams {
   int n_q;      // ceil(Lq / 128) Q tiles
   int Lpad;     // n_q * 128
   int n_items;  // B * Hkv * n_kv
-  int n_pairs;  // B * Hkv * ceil(n_kv / 2): work units of the persistent CTAs
+  int n_units;  // work units of the persistent CTAs (see bwd_unit_item)
+  int ipu;      // K/V tiles per unit: 2 under causal masking, else 1
   float sl2;    // log2(e) / sqrt(D)
   float scale;  // 1 / sqrt(D)
 };
@@ -117,13 +118,20 @@ __device__ __forceinline__ BwdItem bwd_decode(int item, const BwdParams& p) {
   return it;
 }
 
-// Work unit u of the persistent CTAs: K/V tiles j and n_kv-1-j of one
-// (batch, K/V head), the longer first.  Under causal masking tile j visits
-// n_q - j Q tiles (Lq = Lk), so a pair's work is the same for every j; the
-// pairs of one head are consecutive, so the CTAs running at the same time
+// K/V tile s of work unit u of the persistent CTAs.  Under causal masking a
+// unit is the pair of K/V tiles j and n_kv-1-j of one (batch, K/V head), the
+// longer first: tile j visits n_q - j Q tiles (Lq = Lk), so every pair carries
+// the same work (a plain round-robin over single tiles left CTAs with fixed
+// positions j and 50% more work than others).  Without masking every tile is
+// the same work and a unit is one tile (finer units shorten the last round).
+// Units of one head are consecutive, so the CTAs running at the same time
 // share a few heads' Q / dO in L2.  Returns false for the missing second tile
 // of the middle pair when n_kv is odd.
-__device__ __forceinline__ bool bwd_pair_item(int u, int s, const BwdParams& p, int& item) {
+__device__ __forceinline__ bool bwd_unit_item(int u, int s, const BwdParams& p, int& item) {
+  if (p.ipu == 1) {
+    item = u;
+    return true;
+  }
   const int per = (p.n_kv + 1) / 2;
   const int bh = u / per, jp = u - bh * per;
   const int j = s ? p.n_kv - 1 - jp : jp;
@@ -200,7 +208,7 @@ __global__ void __launch_bounds__(512, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  // Persistent CTAs: work units (pairs of K/V tiles, bwd_pair_item)
+  // Persistent CTAs: work units (one or two K/V tiles, bwd_unit_item)
   // blockIdx.x, blockIdx.x + gridDim.x, ...  Every
   // per-tile barrier phase runs on the CTA's tile counter g, so one item's
   // last tiles (dQ drain, dK/dV epilogue) overlap the next item's first ones;
@@ -213,10 +221,10 @@ __global__ void __launch_bounds__(512, 1)
     bool ok = true;
     uint32_t issued[Ly::STAGES] = {0, 0};
     uint32_t stage = 0, phase = 0, kv_cnt = 0;
-    for (int u = 2 * static_cast<int>(blockIdx.x); ok && u < 2 * p.n_pairs;
-         u += (u & 1) ? 2 * G - 1 : 1) {
+    for (int u = p.ipu * static_cast<int>(blockIdx.x); ok && u < p.ipu * p.n_units;
+         u += (u % p.ipu == p.ipu - 1) ? p.ipu * (G - 1) + 1 : 1) {
     int item;
-    if (!bwd_pair_item(u >> 1, u & 1, p, item)) continue;
+    if (!bwd_unit_item(u / p.ipu, u % p.ipu, p, item)) continue;
     const BwdItem it = bwd_decode(item, p);
     if (kv_cnt > 0 && !mbar_wait_warp(bar(Ly::B_KVEMPTY), (kv_cnt - 1) & 1, ab, err, 402)) {
       ok = false;
@@ -287,10 +295,10 @@ __global__ void __launch_bounds__(512, 1)
     const uint64_t dsd = sdesc_sw128(base + Ly::DS_OFF, 16, 1024);
     const uint64_t dsd_mn = sdesc_sw128(base + Ly::DS_OFF, Ly::CHUNK, 1024);
     auto koff = [](int k) -> uint64_t { return ((k >> 2) * Ly::CHUNK + (k & 3) * 32u) >> 4; };
-    for (int u = 2 * static_cast<int>(blockIdx.x); ok && u < 2 * p.n_pairs;
-         u += (u & 1) ? 2 * G - 1 : 1) {
+    for (int u = p.ipu * static_cast<int>(blockIdx.x); ok && u < p.ipu * p.n_units;
+         u += (u % p.ipu == p.ipu - 1) ? p.ipu * (G - 1) + 1 : 1) {
     int item;
-    if (!bwd_pair_item(u >> 1, u & 1, p, item)) continue;
+    if (!bwd_unit_item(u / p.ipu, u % p.ipu, p, item)) continue;
     const BwdItem it = bwd_decode(item, p);
     if (!mbar_wait_warp(bar(Ly::B_KVFULL), kv_cnt & 1, ab, err, 501)) { ok = false; break; }
     tc_fence_after();
@@ -393,10 +401,10 @@ __global__ void __launch_bounds__(512, 1)
     const float sl2 = p.sl2;
     bool ok = true;
     uint32_t stage = 0, g = 0, kv_cnt = 0;
-    for (int u = 2 * static_cast<int>(blockIdx.x); ok && u < 2 * p.n_pairs;
-         u += (u & 1) ? 2 * G - 1 : 1) {
+    for (int u = p.ipu * static_cast<int>(blockIdx.x); ok && u < p.ipu * p.n_units;
+         u += (u % p.ipu == p.ipu - 1) ? p.ipu * (G - 1) + 1 : 1) {
     int item;
-    if (!bwd_pair_item(u >> 1, u & 1, p, item)) continue;
+    if (!bwd_unit_item(u / p.ipu, u % p.ipu, p, item)) continue;
     const BwdItem it = bwd_decode(item, p);
     const int kr = it.j * 128 + r;
     for (int n = 0; ok && n < it.ntiles; ++n, ++g) {
@@ -507,10 +515,10 @@ __global__ void __launch_bounds__(512, 1)
     const uint32_t lane_off = ((warp & 3u) * 32u) << 16;
     bool ok = true;
     uint32_t g = 0;
-    for (int u = 2 * static_cast<int>(blockIdx.x); ok && u < 2 * p.n_pairs;
-         u += (u & 1) ? 2 * G - 1 : 1) {
+    for (int u = p.ipu * static_cast<int>(blockIdx.x); ok && u < p.ipu * p.n_units;
+         u += (u % p.ipu == p.ipu - 1) ? p.ipu * (G - 1) + 1 : 1) {
     int item;
-    if (!bwd_pair_item(u >> 1, u & 1, p, item)) continue;
+    if (!bwd_unit_item(u / p.ipu, u % p.ipu, p, item)) continue;
     const BwdItem it = bwd_decode(item, p);
     for (int n = 0; n < it.ntiles; ++n, ++g) {
       int h, i;
