@@ -26,15 +26,16 @@
 //              vector reductions (the second half's paced).
 //   warp  12   TMA producer: K_j, V_j once per K/V tile; then Q_i, dO_i (and
 //              LSE_i, Delta_i) through a two-slot ring.
-//   warp  13   TMEM allocator and the single tcgen05.mma issuing thread.
+//   warp  13   TMEM allocator and MMA issuer (the warp runs the schedule,
+//              one elected lane issues the MMAs and their commits).
 //   warps 14-15 idle.
-// Per tile the MMA thread issues dP^T for query half A, S^T for all 128
-// queries, then dP^T for half B, so warpgroup A exponentiates while the
-// tensor core computes half B's dP^T (and half A's dV/dK products run while
-// warpgroup B finishes); S^T and dQ are single N=128 MMA groups, keeping the
-// instruction count per tile at 48.  dK and dV stay in TMEM for the whole CTA;
-// for grouped-query attention the CTA loops over every query head of its K/V
-// head, so dK/dV need no atomics.
+// Per tile the MMA warp issues dP^T for query half A, S^T for all 128
+// queries, then dP^T for half B, so the compute warps exponentiate half A
+// while the tensor core computes half B's dP^T (and half A's dV/dK products
+// run while they finish half B); S^T and dQ are single N=128 MMA groups,
+// keeping the instruction count per tile at 48.  dK and dV stay in TMEM for a
+// whole K/V tile; for grouped-query attention the CTA loops over every query
+// head of its K/V head, so dK/dV need no atomics.
 #pragma once
 
 #include <cuda_bf16.h>

@@ -13,7 +13,8 @@
 //   warps 0-3  softmax warpgroup for Q tile 0 (thread i owns row i)
 //   warps 4-7  softmax warpgroup for Q tile 1
 //   warp  8    TMA producer: Q pair, then (V_{j-1}, K_j) tile pairs into a ring
-//   warp  9    TMEM allocator and the single tcgen05.mma issuing thread
+//   warp  9    TMEM allocator and MMA issuer (the warp runs the schedule,
+//              one elected lane issues the MMAs and their commits)
 // Registers are not re-balanced between warps (no setmaxnreg): a fixed split
 // depends on the launch allocation and would wait forever if a tool or
 // compiler changed it; the softmax instead stays within the uniform budget.
