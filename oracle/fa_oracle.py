@@ -46,6 +46,31 @@ softmax, no fusion):
   and the preprocess reads that tensor; ``o_round`` lets the backward round
   its own O to that storage format before forming Delta (None = exact O).
 
+* The dV product: the main backward kernel of the same page (section
+  算子拆分与流水线设计) casts the transposed probabilities to the input type
+  before the dV GEMM (its qkT_cast operand), as the forward page casts P
+  before the PV GEMM; ``p_round`` lets the backward round P to that storage
+  format for the dV product only (None = exact P).
+
+* The forward's cast: the forward kernel of "使用 TileLang 在 AMD GPU 上快速
+  开发高性能 Flash Attention" (section K/V Tile 遍历与核心计算; the buffer is
+  allocated in the input type in section Q Tile 处理与缓存初始化) copies the
+  exponentiated score tile into that buffer before multiplying it with V,
+  and divides by the row sum only when it writes the output.  ``unit_forward``'s ``p_round``
+  rounds the unnormalised exp(S - m) (m the row max; the row sum stays
+  unrounded) to that format before the PV product; the backward's
+  ``fwd_p_round`` forms the O behind Delta the same way.  Reading taken
+  here: the tile is cast relative to the final row max; an online kernel
+  casts it relative to its running max, which is the same value for rows
+  whose maximum lies in the first key tile they visit and otherwise only
+  moves which way each value rounds.
+
+* The dK and dQ products: the pages print no cast of dS, but every GEMM in
+  their kernels multiplies tiles of the input type, and the backward casts
+  its transposed probabilities (the dV operand) to it.  Reading taken here:
+  dS is cast the same way before its two GEMMs; ``ds_round`` rounds dS to
+  that format for the dK and dQ products only (None = exact dS).
+
 * Backward (the page elides every step after the dV product): the analytic
   gradient of O = softmax(S) V,
 
@@ -149,12 +174,21 @@ def _softmax_rows(S: np.ndarray):
     return E / s, m[:, 0], s[:, 0]
 
 
-def unit_forward(q_bh, k_bh, v_bh, causal: bool, rows=None, panel: int = 4096):
+def _output(S, P, m, s, v_bh, p_round):
+    """O = P V, or with the unnormalised tile cast first: cast(exp(S - m)) V / s."""
+    if p_round is None:
+        return P @ v_bh
+    return (storage_round(np.exp(S - m[:, None]), p_round) @ v_bh) / s[:, None]
+
+
+def unit_forward(q_bh, k_bh, v_bh, causal: bool, rows=None, panel: int = 4096, p_round=None):
     """O and LSE rows of one (b, h).
 
     q_bh [Lq, D], k_bh / v_bh [Lk, D] (already the K/V head this query head
     reads), Lq <= Lk under causal masking.  ``rows`` (optional int array)
     restricts the output to those query rows; the keys are always all Lk.
+    ``p_round`` (None, "fp16", "bf16"): the format exp(S - m) is cast to
+    before the PV product, O = cast(exp(S - m)) V / sum_j exp(S_ij - m_i).
     Returns (O [n, D], LSE [n]).
     """
     q_bh, k_bh, v_bh = _as64(q_bh), _as64(k_bh), _as64(v_bh)
@@ -168,21 +202,25 @@ def unit_forward(q_bh, k_bh, v_bh, causal: bool, rows=None, panel: int = 4096):
         if causal:
             S = np.where(np.arange(Lk)[None, :] > r[:, None] + past, -np.inf, S)
         P, m, s = _softmax_rows(S)
-        outs_o.append(P @ v_bh)
+        outs_o.append(_output(S, P, m, s, v_bh, p_round))
         outs_l.append(m + np.log(s))
     if not outs_o:
         return np.zeros((0, q_bh.shape[1])), np.zeros((0,))
     return np.concatenate(outs_o), np.concatenate(outs_l)
 
 
-def unit_backward(q_bh, k_bh, v_bh, do_bh, causal: bool, panel: int = 4096, o_round=None):
+def unit_backward(q_bh, k_bh, v_bh, do_bh, causal: bool, panel: int = 4096, o_round=None,
+                  p_round=None, ds_round=None, fwd_p_round=None):
     """Gradients of one (b, h) pair against its K/V head.
 
     q_bh, do_bh [Lq, D]; k_bh, v_bh [Lk, D] (Lq <= Lk under causal masking).
     Returns (dQ [Lq, D], dK [Lk, D], dV [Lk, D], Delta [Lq], O [Lq, D], LSE [Lq]).
     The oracle recomputes its own O and Delta; nothing comes from a kernel.
-    ``o_round`` (None, "fp16", "bf16") is the storage format of the O that
-    Delta is formed from.
+    Formats (None, "fp16", "bf16"): ``o_round`` is the storage format of the
+    O that Delta is formed from and ``fwd_p_round`` the forward's cast of
+    exp(S - m) that made that O; ``p_round`` the format P is cast to for the
+    dV product; ``ds_round`` the format dS is cast to for the dK and dQ
+    products.  The returned O is the exact one.
     """
     q_bh, k_bh, v_bh, do_bh = (_as64(x) for x in (q_bh, k_bh, v_bh, do_bh))
     Lq, D = q_bh.shape
@@ -205,21 +243,23 @@ def unit_backward(q_bh, k_bh, v_bh, do_bh, causal: bool, panel: int = 4096, o_ro
         o[r] = O
         lse[r] = m + np.log(s)
         dO = do_bh[r]
-        dl = (storage_round(O, o_round) * dO).sum(axis=1)   # Delta_i = sum_d O_id dO_id
+        Os = storage_round(_output(S, P, m, s, v_bh, fwd_p_round), o_round)  # stored O
+        dl = (Os * dO).sum(axis=1)              # Delta_i = sum_d O_id dO_id
         delta[r] = dl
-        dv += P.T @ dO                          # dV = P^T dO
+        dv += storage_round(P, p_round).T @ dO  # dV = P^T dO (P cast for the product)
         dP = dO @ v_bh.T                        # dP = dO V^T
         dS = P * (dP - dl[:, None])             # dS = P o (dP - Delta)
+        dS = storage_round(dS, ds_round)        # (dS cast for its two products)
         dq[r] = (dS @ k_bh) * inv               # dQ = dS K / sqrt(D)
         dk += (dS.T @ q_bh[r]) * inv            # dK = dS^T Q / sqrt(D)
     return dq, dk, dv, delta, o, lse
 
 
-def forward(q, k, v, causal: bool):
+def forward(q, k, v, causal: bool, p_round=None):
     """Full forward over BSHD tensors.
 
     q [B, Lq, H, D]; k, v [B, Lk, Hkv, D].  Returns O [B, Lq, H, D] and
-    LSE [B, H, Lq] (float64).
+    LSE [B, H, Lq] (float64); ``p_round`` as in ``unit_forward``.
     """
     q, k, v = _as64(q), _as64(k), _as64(v)
     B, L, H, D = q.shape
@@ -230,7 +270,7 @@ def forward(q, k, v, causal: bool):
         for h in range(H):
             hk = kv_head(h, H, Hkv)
             o[b, :, h, :], lse[b, h, :] = unit_forward(
-                q[b, :, h, :], k[b, :, hk, :], v[b, :, hk, :], causal)
+                q[b, :, h, :], k[b, :, hk, :], v[b, :, hk, :], causal, p_round=p_round)
     return o, lse
 
 
@@ -240,12 +280,13 @@ def bwd_preprocess(o, do):
     return np.einsum("blhd,blhd->bhl", o, do)
 
 
-def backward(q, k, v, do, causal: bool, o_round=None):
+def backward(q, k, v, do, causal: bool, o_round=None, p_round=None, ds_round=None,
+             fwd_p_round=None):
     """Full backward over BSHD tensors.
 
     q, do [B, Lq, H, D]; k, v [B, Lk, Hkv, D].  Returns dQ [B, Lq, H, D],
     dK [B, Lk, Hkv, D], dV [B, Lk, Hkv, D], Delta [B, H, Lq] (from the
-    oracle's own O, rounded to ``o_round`` if given).
+    oracle's own O).  The format options are those of ``unit_backward``.
     """
     q, k, v, do = _as64(q), _as64(k), _as64(v), _as64(do)
     B, L, H, D = q.shape
@@ -259,7 +300,7 @@ def backward(q, k, v, do, causal: bool, o_round=None):
             hk = kv_head(h, H, Hkv)
             gq, gk, gv, dl, _, _ = unit_backward(
                 q[b, :, h, :], k[b, :, hk, :], v[b, :, hk, :], do[b, :, h, :], causal,
-                o_round=o_round)
+                o_round=o_round, p_round=p_round, ds_round=ds_round, fwd_p_round=fwd_p_round)
             dq[b, :, h, :] = gq
             dk[b, :, hk, :] += gk                 # group heads sum into their KV head
             dv[b, :, hk, :] += gv

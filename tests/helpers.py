@@ -13,6 +13,13 @@ ATOL = 1e-2
 LSE_ATOL = 1e-3
 
 
+def kernel_casts(dtype):
+    """Oracle backward options for the 16-bit casts the method puts before its GEMMs:
+    the forward's exp(S - m) tile and the stored O behind Delta, P^T before dV, dS
+    before dK and dQ."""
+    return dict(o_round=dtype, fwd_p_round=dtype, p_round=dtype, ds_round=dtype)
+
+
 def assert_close(got, ref, rtol=RTOL, atol=ATOL, name="x"):
     got = np.asarray(got, dtype=np.float64)
     ref = np.asarray(ref, dtype=np.float64)

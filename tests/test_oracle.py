@@ -440,6 +440,151 @@ def test_rounded_delta_only_moves_delta():
     assert np.abs(d1 - d0).max() > 0
 
 
+@pytest.mark.parametrize("fmt,tdt", [("bf16", torch.bfloat16), ("fp16", torch.float16)])
+def test_cast_p_only_moves_dv(fmt, tdt):
+    # P cast for the dV product: dV equals P (torch's softmax, cast by torch) times dO;
+    # dQ, dK and Delta are those of the exact P.
+    B, L, H, Hkv, D = 1, 33, 4, 2, 16
+    q, k, v, do = (rnd((B, L, h, D), s) for h, s in ((H, 90), (Hkv, 91), (Hkv, 92), (H, 93)))
+    dq0, dk0, dv0, d0 = orc.backward(q, k, v, do, True)
+    dq1, dk1, dv1, d1 = orc.backward(q, k, v, do, True, p_round=fmt)
+    np.testing.assert_array_equal(dq0, dq1)
+    np.testing.assert_array_equal(dk0, dk1)
+    np.testing.assert_array_equal(d0, d1)
+    qt, kt, dot = (torch.from_numpy(x) for x in (q, k, do))
+    mask = torch.ones(L, L, dtype=torch.bool).tril()
+    ref = torch.zeros(B, L, Hkv, D, dtype=torch.float64)
+    for h in range(H):
+        hk = h // (H // Hkv)
+        s = qt[0, :, h] @ kt[0, :, hk].T / math.sqrt(D)
+        p = torch.softmax(s.masked_fill(~mask, float("-inf")), dim=1)
+        ref[0, :, hk] += p.to(torch.float32).to(tdt).double().T @ dot[0, :, h]
+    np.testing.assert_allclose(dv1, ref.numpy(), rtol=1e-12, atol=1e-12)
+    assert np.abs(dv1 - dv0).max() > 0
+
+
+def test_cast_p_exact_when_p_is_representable():
+    # Zero queries: row i of P is 1/L (non-causal, L a power of two) -- exact in 16 bits.
+    B, L, H, D = 1, 32, 2, 8
+    q = np.zeros((B, L, H, D))
+    k, v, do = (rnd((B, L, H, D), s) for s in (94, 95, 96))
+    for fmt in ("bf16", "fp16"):
+        _, _, dv0, _ = orc.backward(q, k, v, do, False)
+        _, _, dv1, _ = orc.backward(q, k, v, do, False, p_round=fmt)
+        np.testing.assert_allclose(dv1, dv0, rtol=0, atol=1e-14)
+
+
+def _torch_unit(qt, kt, vt, dot, h, hk, causal):
+    """Independent float64 torch computation of one (b=0, h) unit: S, E = exp(S - m),
+    row sum l, P, dP, exact O."""
+    L, D = qt.shape[1], qt.shape[3]
+    s = qt[0, :, h] @ kt[0, :, hk].T / math.sqrt(D)
+    if causal:
+        s = s.masked_fill(~torch.ones(L, L, dtype=torch.bool).tril(), float("-inf"))
+    m = s.max(dim=1, keepdim=True).values
+    e = torch.exp(s - m)
+    l = e.sum(dim=1, keepdim=True)
+    p = e / l
+    return e, l, p, dot[0, :, h] @ vt[0, :, hk].T, p @ vt[0, :, hk]
+
+
+@pytest.mark.parametrize("fmt,tdt", [("bf16", torch.bfloat16), ("fp16", torch.float16)])
+@pytest.mark.parametrize("causal", [False, True])
+def test_forward_cast_matches_torch(fmt, tdt, causal):
+    # O = cast(exp(S - m)) V / l with l the unrounded row sum; LSE is unchanged.
+    B, L, H, Hkv, D = 1, 37, 4, 2, 16
+    q, k, v = (rnd((B, L, h, D), s) for h, s in ((H, 100), (Hkv, 101), (Hkv, 102)))
+    o0, lse0 = orc.forward(q, k, v, causal)
+    o1, lse1 = orc.forward(q, k, v, causal, p_round=fmt)
+    np.testing.assert_array_equal(lse0, lse1)
+    qt, kt, vt = (torch.from_numpy(x) for x in (q, k, v))
+    for h in range(H):
+        hk = h // (H // Hkv)
+        e, l, _, _, _ = _torch_unit(qt, kt, vt, qt, h, hk, causal)
+        want = (e.to(torch.float32).to(tdt).double() @ vt[0, :, hk]) / l
+        np.testing.assert_allclose(o1[0, :, h], want.numpy(), rtol=1e-12, atol=1e-12)
+    # the cast moves O by at most half an ulp of each weight: |dO| <= u sum_j P_j |V_j|
+    u = {"bf16": 2.0 ** -8, "fp16": 2.0 ** -11}[fmt]
+    p = np.stack([_torch_unit(qt, kt, vt, qt, h, h // (H // Hkv), causal)[2].numpy()
+                  for h in range(H)], axis=1)                     # [L, H, L]
+    bound = u * np.einsum("ihj,jhd->ihd", p, np.abs(np.repeat(v[0], H // Hkv, axis=1)))
+    assert np.all(np.abs(o1[0] - o0[0]) <= bound + 1e-15)
+    assert np.abs(o1 - o0).max() > 0
+
+
+def test_forward_cast_exact_when_weights_are_representable():
+    # Zero queries: exp(S - m) = 1 on every visible key, exact in 16 bits.
+    B, L, H, D = 1, 32, 2, 8
+    q = np.zeros((B, L, H, D))
+    k, v = (rnd((B, L, H, D), s) for s in (103, 104))
+    for causal in (False, True):
+        o0, _ = orc.forward(q, k, v, causal)
+        for fmt in ("bf16", "fp16"):
+            o1, _ = orc.forward(q, k, v, causal, p_round=fmt)
+            np.testing.assert_allclose(o1, o0, rtol=0, atol=1e-14)
+
+
+@pytest.mark.parametrize("fmt,tdt", [("bf16", torch.bfloat16), ("fp16", torch.float16)])
+def test_cast_ds_only_moves_dq_dk(fmt, tdt):
+    # dS cast for the dK and dQ products: dQ = cast(dS) K / sqrt(D), dK = sum over the
+    # group of cast(dS)^T Q / sqrt(D), dS from torch's softmax; dV and Delta unchanged.
+    B, L, H, Hkv, D = 1, 35, 4, 2, 12   # 1/sqrt(12) is no power of two: the cast precedes it
+    q, k, v, do = (rnd((B, L, h, D), s) for h, s in ((H, 105), (Hkv, 106), (Hkv, 107), (H, 108)))
+    dq0, dk0, dv0, d0 = orc.backward(q, k, v, do, True)
+    dq1, dk1, dv1, d1 = orc.backward(q, k, v, do, True, ds_round=fmt)
+    np.testing.assert_array_equal(dv0, dv1)
+    np.testing.assert_array_equal(d0, d1)
+    qt, kt, vt, dot = (torch.from_numpy(x) for x in (q, k, v, do))
+    want_dk = torch.zeros(B, L, Hkv, D, dtype=torch.float64)
+    for h in range(H):
+        hk = h // (H // Hkv)
+        _, _, p, dp, o = _torch_unit(qt, kt, vt, dot, h, hk, True)
+        delta = (o * dot[0, :, h]).sum(dim=1, keepdim=True)
+        ds = (p * (dp - delta)).to(torch.float32).to(tdt).double()
+        np.testing.assert_allclose(dq1[0, :, h], (ds @ kt[0, :, hk] / math.sqrt(D)).numpy(),
+                                   rtol=1e-12, atol=1e-12)
+        want_dk[0, :, hk] += ds.T @ qt[0, :, h] / math.sqrt(D)
+    np.testing.assert_allclose(dk1, want_dk.numpy(), rtol=1e-12, atol=1e-12)
+    assert np.abs(dk1 - dk0).max() > 0 and np.abs(dq1 - dq0).max() > 0
+
+
+@pytest.mark.parametrize("zero", ["q", "k"])
+def test_cast_ds_exact_when_ds_is_representable(zero):
+    # Zero queries or zero keys, L = 8 keys (P = 1/8), V and dO in {0, 1}, D = 4: dP is
+    # an integer, Delta a multiple of 1/8 below 4, so dS = (dP - Delta)/8 has at most 6
+    # significant bits -- exact in bf16 and fp16.  Zero queries leave dQ = dS K nonzero,
+    # zero keys dK = dS^T Q.
+    B, L, H, D = 1, 8, 2, 4
+    rng = np.random.default_rng(109)
+    q, k = (rng.standard_normal((B, L, H, D)) for _ in range(2))
+    (q if zero == "q" else k)[:] = 0.0
+    v, do = (rng.integers(0, 2, (B, L, H, D)).astype(np.float64) for _ in range(2))
+    ref = orc.backward(q, k, v, do, False)
+    assert np.abs(ref[0 if zero == "q" else 1]).max() > 0
+    for fmt in ("bf16", "fp16"):
+        got = orc.backward(q, k, v, do, False, ds_round=fmt)
+        for a, b in zip(ref, got):
+            np.testing.assert_allclose(b, a, rtol=0, atol=1e-14)
+
+
+@pytest.mark.parametrize("fmt,tdt", [("bf16", torch.bfloat16), ("fp16", torch.float16)])
+def test_forward_cast_in_backward_moves_delta(fmt, tdt):
+    # fwd_p_round forms the O behind Delta with the forward's cast: Delta is the row dot
+    # product of (cast(exp(S - m)) V / l, stored) with dO; dV does not depend on Delta.
+    B, L, H, D = 1, 30, 2, 16
+    q, k, v, do = (rnd((B, L, H, D), s) for s in (110, 111, 112, 113))
+    _, _, dv0, d0 = orc.backward(q, k, v, do, True)
+    _, _, dv1, d1 = orc.backward(q, k, v, do, True, o_round=fmt, fwd_p_round=fmt)
+    np.testing.assert_array_equal(dv0, dv1)
+    qt, kt, vt, dot = (torch.from_numpy(x) for x in (q, k, v, do))
+    for h in range(H):
+        e, l, _, _, _ = _torch_unit(qt, kt, vt, dot, h, h, True)
+        o = ((e.to(torch.float32).to(tdt).double() @ vt[0, :, h]) / l).to(torch.float32).to(tdt)
+        want = (o.double() * dot[0, :, h]).sum(dim=1)
+        np.testing.assert_allclose(d1[0, h], want.numpy(), rtol=1e-12, atol=1e-12)
+    assert np.abs(d1 - d0).max() > 0
+
+
 # ---------------------------------------------------------------- fewer queries than keys
 
 def _suffix_case(seed, B=1, L=23, Lq=7, H=2, Hkv=1, D=8):
