@@ -8,7 +8,7 @@ import pytest
 import torch
 
 import tiled_attention_fa_gb300 as fa
-from tests.helpers import assert_close, inputs, to64
+from tests.helpers import assert_close, inputs, kernel_casts, to64
 from oracle import fa_oracle as orc
 
 pytestmark = pytest.mark.gpu
@@ -26,8 +26,9 @@ def run_and_compare(B, L, H, Hkv, D, dtype, causal, seed):
     (q, k, v, do), (qd, kd, vd, dod) = inputs(B, L, H, Hkv, D, dtype, seed)
     o, lse, dq, dk, dv, delta = gpu_fwd_bwd(qd, kd, vd, dod, causal)
     # Delta is formed from the stored O (input dtype), as the preprocess stage
-    # reads the forward's output tensor; the oracle rounds its own O likewise.
-    rq, rk, rv, rdelta = orc.backward(q, k, v, do, causal, o_round=dtype)
+    # reads the forward's output tensor; the oracle rounds its own O likewise,
+    # and casts P to the input type for the dV product as the method does.
+    rq, rk, rv, rdelta = orc.backward(q, k, v, do, causal, **kernel_casts(dtype))
     assert_close(to64(dv), rv, name="dV")
     assert_close(to64(dk), rk, name="dK")
     assert_close(to64(dq), rq, name="dQ")
@@ -79,7 +80,7 @@ def test_unzeroed_accumulator_path(cuda_lib):
     delta = fa.bwd_preprocess(o, dod)
     acc = torch.full((fa.workspace_size(1, 256, 2, 64) // 4,), 3.0, device="cuda")
     dq, dk, dv = fa.bwd(qd, kd, vd, o, dod, lse, delta, True, dq_accum=acc, accum_zeroed=False)
-    rq, rk, rv, _ = orc.backward(q, k, v, do, True, o_round="fp16")
+    rq, rk, rv, _ = orc.backward(q, k, v, do, True, **kernel_casts("fp16"))
     assert_close(to64(dq), rq, name="dQ")
     assert_close(to64(dk), rk, name="dK")
     assert_close(to64(dv), rv, name="dV")

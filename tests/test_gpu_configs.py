@@ -12,7 +12,7 @@ import torch
 
 import tiled_attention_fa_gb300 as fa
 from oracle import fa_oracle as orc
-from tests.helpers import LSE_ATOL, assert_close
+from tests.helpers import LSE_ATOL, assert_close, kernel_casts
 from tiled_attention_fa_gb300.inputs import make_qkv
 
 pytestmark = pytest.mark.gpu
@@ -38,7 +38,8 @@ def check_bwd_units(q, k, v, do, dq, dk, dv, causal, units, dtype):
     dq, dk, dv = dq.cpu(), dk.cpu(), dv.cpu()
     for b, h in units:
         rq, rk, rv, _, _, _ = orc.unit_backward(unit64(q, b, h), unit64(k, b, h), unit64(v, b, h),
-                                                unit64(do, b, h), causal, panel=2048, o_round=dtype)
+                                                unit64(do, b, h), causal, panel=2048,
+                                                **kernel_casts(dtype))
         assert_close(unit64(dv, b, h), rv, name=f"dV[{b},:,{h}]")
         assert_close(unit64(dk, b, h), rk, name=f"dK[{b},:,{h}]")
         assert_close(unit64(dq, b, h), rq, name=f"dQ[{b},:,{h}]")

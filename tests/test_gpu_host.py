@@ -1,6 +1,6 @@
 """Host-buffer entry points: HostRunner (one step) and HostPipeline (steps
-whose copies overlap their neighbours' kernels) return exactly what the
-device-side calls return on the same inputs."""
+whose copies overlap their neighbours' kernels) return what the device-side
+calls return on the same inputs (bit for bit, except dQ's last place)."""
 
 import pytest
 import torch
@@ -20,8 +20,13 @@ def device_reference(q, k, v, do, causal):
 
 
 def same(got, ref):
-    for name in ("o", "lse", "dq", "dk", "dv"):
+    # O, LSE, dK, dV are formed in a fixed order and match bit for bit.  dQ is
+    # summed in fp32 by reductions from many CTAs in hardware order before its
+    # 16-bit rounding, so it may differ by one unit in the last place.
+    for name in ("o", "lse", "dk", "dv"):
         assert torch.equal(got[name], ref[name]), name
+    a, b = got["dq"].double(), ref["dq"].double()
+    assert torch.all((a - b).abs() <= 2.0 ** -7 * b.abs() + 1e-6), "dq"
 
 
 @pytest.mark.parametrize("causal", [False, True])
