@@ -17,25 +17,26 @@
 //              of key rows 32*(w%4).. (its TMEM lanes); a thread owns one
 //              key row and forms
 //              P^T = exp2(S^T*c - LSE*log2e) and dS^T = P^T o (dP^T - Delta);
-//              P^T goes back to TMEM (A operand of dV += P^T dO), dS^T to a
-//              swizzled smem tile (A operand of dK += dS^T Q and, read
-//              MN-major, of dQ = dS K).  At the end warps 0-3 write dK and
-//              warps 4-7 dV.
-//   warps 8-11 dQ drain: thread r owns query row r; reads the dQ tile from
-//              TMEM and adds it into the fp32 accumulator with 16-byte
-//              vector reductions (the second half's paced).
+//              both go back to TMEM over the chunk's S^T columns (A operands
+//              of dV += P^T dO and dK += dS^T Q) and dS^T also to a swizzled
+//              smem tile (read MN-major as the A operand of dQ = dS K).  At
+//              the end warps 0-3 write dK and warps 4-7 dV.
+//   warps 8-11 dQ drain: thread r owns query row r; takes the whole dQ row
+//              from TMEM, releases the columns, then adds it into the fp32
+//              accumulator with paced 16-byte vector reductions.
 //   warp  12   TMA producer: K_j, V_j once per K/V tile; then Q_i, dO_i (and
 //              LSE_i, Delta_i) through a two-slot ring.
 //   warp  13   TMEM allocator and MMA issuer (the warp runs the schedule,
 //              one elected lane issues the MMAs and their commits).
-//   warps 14-15 idle.
-// Per tile the MMA warp issues dP^T for query half A, S^T for all 128
-// queries, then dP^T for half B, so the compute warps exponentiate half A
-// while the tensor core computes half B's dP^T (and half A's dV/dK products
-// run while they finish half B); S^T and dQ are single N=128 MMA groups,
-// keeping the instruction count per tile at 48.  dK and dV stay in TMEM for a
-// whole K/V tile; for grouped-query attention the CTA loops over every query
-// head of its K/V head, so dK/dV need no atomics.
+//   warps 14-15 idle (they only lower their register budget with 12-13).
+// An MMA with both operands in shared memory reads them at the shared-memory
+// rate (128 B per clock: an M=128 N=128 K=16 step, 8 KB, takes its 64 tensor
+// cycles in reads alone), so the schedule keeps every operand it can in TMEM:
+// per tile S^T and dP^T (both operands in shared memory, N = 128 queries),
+// dV and dK (A from TMEM), dQ (both in shared memory): 40 MMAs, 256 KB of
+// operand reads.  dK and dV stay in TMEM for a whole K/V tile; for
+// grouped-query attention the CTA loops over every query head of its K/V
+// head, so dK/dV need no atomics.
 #pragma once
 
 #include <cuda_bf16.h>
@@ -44,6 +45,18 @@
 #include "common.cuh"
 #include "fwd.cuh"  // pack2
 #include "ptx.cuh"
+
+// Pacing of the dQ drain's reductions at D = 128: a pause of FA_BWD_PACE_NS
+// after every FA_BWD_PACE_EVERY reductions (see the drain).
+#ifndef FA_BWD_PACE_NS
+#define FA_BWD_PACE_NS 50
+#endif
+#ifndef FA_BWD_PACE_EVERY
+#define FA_BWD_PACE_EVERY 1
+#endif
+#ifndef FA_BWD_PACE_D64
+#define FA_BWD_PACE_D64 1
+#endif
 
 namespace fa {
 
@@ -74,8 +87,9 @@ struct BwdLayout {
   // Small region first (barriers, TMEM address, abort flag, LSE/Delta slots),
   // then the 1024-byte aligned operand tiles.
   static constexpr int B_KVFULL = 0, B_QFULL = 1, B_QEMPTY = 1 + STAGES, B_SFULL = 1 + 2 * STAGES,
-                       B_PFULL = B_SFULL + 2, B_DQFULL = B_PFULL + 2, B_DQEMPTY = B_DQFULL + 1,
-                       B_DKVFULL = B_DQEMPTY + 2, B_DONE = B_DKVFULL + 1, B_KVEMPTY = B_DONE + 1,
+                       B_DPFULL = B_SFULL + 1, B_PFULL = B_DPFULL + 1, B_DSFULL = B_PFULL + 2,
+                       B_DQFULL = B_DSFULL + 2, B_DQEMPTY = B_DQFULL + 1,
+                       B_DKVFULL = B_DQEMPTY + 1, B_DONE = B_DKVFULL + 1, B_KVEMPTY = B_DONE + 1,
                        NBAR = B_KVEMPTY + 1;
   static constexpr uint32_t BAR_OFF = 0;
   static constexpr uint32_t MISC_OFF = BAR_OFF + NBAR * 8;              // tmem slot, abort flag
@@ -88,15 +102,13 @@ struct BwdLayout {
   static constexpr uint32_t DO_OFF = Q_OFF + STAGES * TILE;   // [STAGES] tiles
   static constexpr uint32_t DS_OFF = DO_OFF + STAGES * TILE;  // 2 chunks (128 keys x 128 queries)
   static constexpr uint32_t SMEM_ALLOC = DS_OFF + 2 * CHUNK;
-  // TMEM columns: dK | dV | dP^T (queries 0-63) | S^T (128 queries) | dP^T (64-127).
-  // The dQ tile (N = D) is written at column 384: at D=64 that is its own
-  // region; at D=128 it covers S^T's query-half-B columns and the second dP^T
-  // half, so the next tile's first MMA (dP^T of half A) never waits for the dQ
-  // drain; each 64-column dQ half is released on its own barrier.
-  static constexpr uint32_t TM_DK = 0, TM_DV = D, TM_DPA = 2 * D, TM_S = 2 * D + 64,
-                            TM_DPB = 2 * D + 192;
-  static constexpr int NDQ = D / 64;
-  __host__ __device__ static constexpr uint32_t tm_dq(int h) { return 384u + 64u * h; }
+  // TMEM columns: dK | dV | S^T (128 queries) | dP^T (128 queries).  The
+  // compute warps overwrite each 32-query chunk of S^T with P^T (16 columns of
+  // 16-bit pairs) and dS^T (the next 16), the A operands of the dV and dK
+  // products.  The dQ tile (N = D) goes into the dP^T columns once both query
+  // halves are consumed; the next tile's S^T never waits for the dQ drain,
+  // only its dP^T does.
+  static constexpr uint32_t TM_DK = 0, TM_DV = D, TM_S = 2 * D, TM_DP = 2 * D + 128;
   static constexpr uint32_t TMEM_COLS = 512;
   static constexpr int NTHREADS = 512;
 };
@@ -157,9 +169,8 @@ __global__ void __launch_bounds__(512, 1)
                   const BwdParams p) {
   using Ly = BwdLayout<D>;
   using T = typename std::conditional<BF16, __nv_bfloat16, __half>::type;
-  constexpr uint32_t IDESC_S = idesc_f16(BF16, 128, 128, false, false);  // S^T, all queries
-  constexpr uint32_t IDESC_DP = idesc_f16(BF16, 128, 64, false, false);  // dP^T, one query half
-  constexpr uint32_t IDESC_KN = idesc_f16(BF16, 128, D, false, true);    // dV (A tmem), dK
+  constexpr uint32_t IDESC_S = idesc_f16(BF16, 128, 128, false, false);  // S^T, dP^T
+  constexpr uint32_t IDESC_KN = idesc_f16(BF16, 128, D, false, true);    // dV, dK (A in TMEM)
   constexpr uint32_t IDESC_MN = idesc_f16(BF16, 128, D, true, true);     // dQ
 
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -183,13 +194,14 @@ __global__ void __launch_bounds__(512, 1)
       mbar_init(bar(Ly::B_QFULL + s), 1);
       mbar_init(bar(Ly::B_QEMPTY + s), 1);
     }
-    for (int c = 0; c < 2; ++c) {
-      mbar_init(bar(Ly::B_SFULL + c), 1);
-      mbar_init(bar(Ly::B_PFULL + c), 8);  // one arrival per compute warp
+    mbar_init(bar(Ly::B_SFULL), 1);
+    mbar_init(bar(Ly::B_DPFULL), 1);
+    for (int c = 0; c < 2; ++c) {  // one arrival per compute warp
+      mbar_init(bar(Ly::B_PFULL + c), 8);
+      mbar_init(bar(Ly::B_DSFULL + c), 8);
     }
     mbar_init(bar(Ly::B_DQFULL), 1);
     mbar_init(bar(Ly::B_DQEMPTY), 4);  // one arrival per drain warp
-    mbar_init(bar(Ly::B_DQEMPTY + 1), 4);
     mbar_init(bar(Ly::B_DKVFULL), 1);
     mbar_init(bar(Ly::B_DONE), 1);
     ab->flag = 0;
@@ -216,8 +228,15 @@ __global__ void __launch_bounds__(512, 1)
   // K_j / V_j of the next item load once the last MMA reading the current ones
   // completes (K/V-empty barrier).
   const int G = static_cast<int>(gridDim.x);
+  // At D = 128 the drain warpgroup (warps 8-11) holds a whole 128-column dQ
+  // row in registers; the producer / MMA warpgroup (12-15) needs few.  Budgets
+  // 128 + 128 + 176 + 80 registers per thread of each warpgroup's 128 threads
+  // sum to the launch total of 512 x 128.  Each role sets its budget first
+  // thing in its own branch, so the compiler allocates that branch to it.
+  constexpr bool kSplitRegs = (D == 128);
 
   if (warp == 12) {
+    if constexpr (kSplitRegs) setmaxnreg_dec<80>();
     // ------------------------------------------------------------ producer (whole warp)
     bool ok = true;
     uint32_t issued[Ly::STAGES] = {0, 0};
@@ -279,6 +298,7 @@ __global__ void __launch_bounds__(512, 1)
         if (issued[s] > 0) mbar_wait_drain(bar(Ly::B_QFULL + s), (issued[s] - 1) & 1);
     }
   } else if (warp == 13) {
+    if constexpr (kSplitRegs) setmaxnreg_dec<80>();
     // ------------------------------------------------------------ MMA issuer
     // The whole warp runs the schedule (warp-uniform loop state and operand
     // descriptors); one elected lane issues each MMA group and the commits.
@@ -293,7 +313,6 @@ __global__ void __launch_bounds__(512, 1)
     const uint64_t kd = sdesc_sw128(base + Ly::K_OFF, 16, 1024);
     const uint64_t vd = sdesc_sw128(base + Ly::V_OFF, 16, 1024);
     const uint64_t kd_mn = sdesc_sw128(base + Ly::K_OFF, Ly::CHUNK, 1024);
-    const uint64_t dsd = sdesc_sw128(base + Ly::DS_OFF, 16, 1024);
     const uint64_t dsd_mn = sdesc_sw128(base + Ly::DS_OFF, Ly::CHUNK, 1024);
     auto koff = [](int k) -> uint64_t { return ((k >> 2) * Ly::CHUNK + (k & 3) * 32u) >> 4; };
     for (int u = p.ipu * static_cast<int>(blockIdx.x); ok && u < p.ipu * p.n_units;
@@ -311,24 +330,8 @@ __global__ void __launch_bounds__(512, 1)
       const uint32_t doa = base + Ly::DO_OFF + stage * Ly::TILE;
       const uint64_t qd = sdesc_sw128(qa, 16, 1024), qd_mn = sdesc_sw128(qa, Ly::CHUNK, 1024);
       const uint64_t dod = sdesc_sw128(doa, 16, 1024), dod_mn = sdesc_sw128(doa, Ly::CHUNK, 1024);
-      // dP^T_A = V_j dO_A^T (queries 0-63), S^T = K_j Q_i^T (all queries),
-      // dP^T_B = V_j dO_B^T (queries 64-127).  Half A's softmax starts after
-      // the first two, overlapping dP^T_B and half B's work.
-      // (commit_bar < 0: no commit after the group)
-      auto issue_dp = [&](int c, uint32_t dst, int commit_bar) {
-        if (elect_one()) {
-#pragma unroll
-          for (int k = 0; k < D / 16; ++k)
-            mma_ss(dst, vd + koff(k), dod + koff(k) + c * (8192u >> 4), IDESC_DP, k > 0 ? 1u : 0u);
-          if (commit_bar >= 0) tc_commit(bar(commit_bar));
-        }
-        __syncwarp();
-      };
-      issue_dp(0, tmem + Ly::TM_DPA, -1);
-      if (D == 128 && g > 0) {  // dQ half 0 of the previous tile sits in S^T's upper half
-        if (!mbar_wait_warp(bar(Ly::B_DQEMPTY), (g - 1) & 1, ab, err, 503)) { ok = false; break; }
-        tc_fence_after();
-      }
+      // S^T = K_j Q_i^T: the previous tile's P^T / dS^T in these columns are
+      // read by MMAs issued before, which run first.
       if (elect_one()) {
 #pragma unroll
         for (int k = 0; k < D / 16; ++k)
@@ -336,12 +339,21 @@ __global__ void __launch_bounds__(512, 1)
         tc_commit(bar(Ly::B_SFULL));
       }
       __syncwarp();
-      if (D == 128 && g > 0) {  // dQ half 1 sits in dP^T_B's columns
-        if (!mbar_wait_warp(bar(Ly::B_DQEMPTY + 1), (g - 1) & 1, ab, err, 507)) { ok = false; break; }
+      // dP^T = V_j dO_i^T, once the drain holds the previous dQ tile (which
+      // occupied these columns) in registers.
+      if (g > 0) {
+        if (!mbar_wait_warp(bar(Ly::B_DQEMPTY), (g - 1) & 1, ab, err, 503)) { ok = false; break; }
         tc_fence_after();
       }
-      issue_dp(1, tmem + Ly::TM_DPB, Ly::B_SFULL + 1);
-      // dV += P^T_c dO_c and dK += dS^T_c Q_c as each half's P^T / dS^T lands.
+      if (elect_one()) {
+#pragma unroll
+        for (int k = 0; k < D / 16; ++k)
+          mma_ss(tmem + Ly::TM_DP, vd + koff(k), dod + koff(k), IDESC_S, k > 0 ? 1u : 0u);
+        tc_commit(bar(Ly::B_DPFULL));
+      }
+      __syncwarp();
+      // dV += P^T_c dO_c as each query half's P^T lands in TMEM, dK += dS^T_c
+      // Q_c as its dS^T does (both A operands from TMEM).
 #pragma unroll
       for (int c = 0; c < 2; ++c) {
         if (!mbar_wait_warp(bar(Ly::B_PFULL + c), g & 1, ab, err, 504 + c)) { ok = false; break; }
@@ -352,24 +364,26 @@ __global__ void __launch_bounds__(512, 1)
             mma_ts(tmem + Ly::TM_DV, tmem + Ly::TM_S + 64 * c + (k >> 1) * 32u + (k & 1) * 8u,
                    dod_mn + ((2048u * (4 * c + k)) >> 4), IDESC_KN,
                    (n > 0 || c > 0 || k > 0) ? 1u : 0u);
+        }
+        __syncwarp();
+        if (!mbar_wait_warp(bar(Ly::B_DSFULL + c), g & 1, ab, err, 508 + c)) { ok = false; break; }
+        tc_fence_after();
+        if (elect_one()) {
 #pragma unroll
           for (int k = 0; k < 4; ++k)
-            mma_ss(tmem + Ly::TM_DK, dsd + ((c * Ly::CHUNK + 32u * k) >> 4),
+            mma_ts(tmem + Ly::TM_DK, tmem + Ly::TM_S + 64 * c + (k >> 1) * 32u + 16u + (k & 1) * 8u,
                    qd_mn + ((2048u * (4 * c + k)) >> 4), IDESC_KN,
                    (n > 0 || c > 0 || k > 0) ? 1u : 0u);
         }
         __syncwarp();
       }
       if (!ok) break;
-      if (D != 128 && g > 0) {
-        if (!mbar_wait_warp(bar(Ly::B_DQEMPTY), (g - 1) & 1, ab, err, 506)) { ok = false; break; }
-        tc_fence_after();
-      }
-      // dQ_i = dS K_j   (dS read MN-major from the dS^T tile, K_j MN-major)
+      // dQ_i = dS K_j into the consumed dP^T columns (dS read MN-major from
+      // the dS^T tile in shared memory, K_j MN-major)
       if (elect_one()) {
 #pragma unroll
         for (int k = 0; k < 8; ++k)
-          mma_ss(tmem + Ly::tm_dq(0), dsd_mn + ((2048u * k) >> 4), kd_mn + ((2048u * k) >> 4),
+          mma_ss(tmem + Ly::TM_DP, dsd_mn + ((2048u * k) >> 4), kd_mn + ((2048u * k) >> 4),
                  IDESC_MN, k > 0 ? 1u : 0u);
         tc_commit(bar(Ly::B_DQFULL));
         tc_commit(bar(Ly::B_QEMPTY + stage));
@@ -411,13 +425,13 @@ __global__ void __launch_bounds__(512, 1)
     for (int n = 0; ok && n < it.ntiles; ++n, ++g) {
       int h, i;
       bwd_tile(it, p, n, h, i);
+      if (!mbar_wait_warp(bar(Ly::B_SFULL), g & 1, ab, err, 601)) { ok = false; break; }
+      tc_fence_after();
 #pragma unroll
       for (int hc = 0; hc < 2; ++hc) {
-        if (!mbar_wait_warp(bar(Ly::B_SFULL + hc), g & 1, ab, err, 601)) { ok = false; break; }
-        tc_fence_after();
         const int cbase = 64 * hc + 32 * sub;  // first query column of this chunk
         const uint32_t tS = tmem + lane_off + Ly::TM_S + cbase;
-        const uint32_t tP = tmem + lane_off + (hc ? Ly::TM_DPB : Ly::TM_DPA) + 32 * sub;
+        const uint32_t tP = tmem + lane_off + Ly::TM_DP + cbase;
         const float* st = stats + stage * 256 + cbase;
         const int q0 = i * 128 + cbase;
         // query columns [lo, hi) of this chunk are visible to key kr
@@ -425,27 +439,22 @@ __global__ void __launch_bounds__(512, 1)
         if (kr >= p.Lk) hi = 0;
         if (p.causal) lo = max(0, kr - p.past - q0);
         const bool full = (lo == 0 && hi == 32);
-        uint32_t sv[32], dp[32];
+        // Phase 1, from S^T alone (dP^T may still be in the tensor core):
+        // P^T = exp2(S^T*c - LSE*log2e), two queries per paired instruction.
+        uint32_t sv[32];
         tmem_ld32(tS, sv);
-        tmem_ld32(tP, dp);
         tmem_ld_wait32(sv);
-        tmem_ld_wait32(dp);
-        uint32_t pk[16], dk[16];
-        // Two queries per paired fp32 instruction: exponent argument
-        // S^T*c - LSE*log2e, then dS^T = P^T (dP^T - Delta).
-        const uint4* nl4 = reinterpret_cast<const uint4*>(st);        // -LSE*log2e
-        const uint4* nd4 = reinterpret_cast<const uint4*>(st + 128);  // -Delta
+        uint32_t pk[16];
+        const uint4* nl4 = reinterpret_cast<const uint4*>(st);  // -LSE*log2e
         const uint64_t sl2x2 = f2_pack(sl2, sl2);
 #pragma unroll
         for (int u4 = 0; u4 < 8; ++u4) {
-          const uint4 l4 = nl4[u4], d4 = nd4[u4];
+          const uint4 l4 = nl4[u4];
 #pragma unroll
           for (int e = 0; e < 2; ++e) {
             const int cl = 4 * u4 + 2 * e;
             const uint64_t nl = e ? f2_pack(__uint_as_float(l4.z), __uint_as_float(l4.w))
                                   : f2_pack(__uint_as_float(l4.x), __uint_as_float(l4.y));
-            const uint64_t nd = e ? f2_pack(__uint_as_float(d4.z), __uint_as_float(d4.w))
-                                  : f2_pack(__uint_as_float(d4.x), __uint_as_float(d4.y));
             float a0, a1;
             f2_unpack(ffma2(f2_pack(__uint_as_float(sv[cl]), __uint_as_float(sv[cl + 1])), sl2x2, nl),
                       a0, a1);
@@ -454,17 +463,45 @@ __global__ void __launch_bounds__(512, 1)
               p0 = (cl >= lo && cl < hi) ? p0 : 0.f;
               p1 = (cl + 1 >= lo && cl + 1 < hi) ? p1 : 0.f;
             }
-            const uint64_t pp = f2_pack(p0, p1);
-            float d0, d1;
-            f2_unpack(fmul2(pp, fadd2(f2_pack(__uint_as_float(dp[cl]), __uint_as_float(dp[cl + 1])), nd)),
-                      d0, d1);
+            sv[cl] = __float_as_uint(p0);  // P^T in fp32 for phase 2
+            sv[cl + 1] = __float_as_uint(p1);
             pk[cl >> 1] = pack2<T>(p0, p1);
+          }
+        }
+        // P^T (16-bit pairs) over the first 16 of this chunk's S^T columns.
+        tmem_st16(tS, pk);
+        tmem_st_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(Ly::B_PFULL + hc));
+        // Phase 2: dS^T = P^T o (dP^T - Delta).
+        if (hc == 0) {
+          if (!mbar_wait_warp(bar(Ly::B_DPFULL), g & 1, ab, err, 602)) { ok = false; break; }
+          tc_fence_after();
+        }
+        uint32_t dp[32];
+        tmem_ld32(tP, dp);
+        tmem_ld_wait32(dp);
+        uint32_t dk[16];
+        const uint4* nd4 = reinterpret_cast<const uint4*>(st + 128);  // -Delta
+#pragma unroll
+        for (int u4 = 0; u4 < 8; ++u4) {
+          const uint4 d4 = nd4[u4];
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const int cl = 4 * u4 + 2 * e;
+            const uint64_t nd = e ? f2_pack(__uint_as_float(d4.z), __uint_as_float(d4.w))
+                                  : f2_pack(__uint_as_float(d4.x), __uint_as_float(d4.y));
+            float d0, d1;
+            f2_unpack(fmul2(f2_pack(__uint_as_float(sv[cl]), __uint_as_float(sv[cl + 1])),
+                            fadd2(f2_pack(__uint_as_float(dp[cl]), __uint_as_float(dp[cl + 1])), nd)),
+                      d0, d1);
             dk[cl >> 1] = pack2<T>(d0, d1);
           }
         }
-        // P^T (16-bit pairs) over the first 16 of this chunk's own S^T columns.
-        tmem_st16(tS, pk);
-        // dS^T row r, queries cbase .. cbase+31: four swizzled 16-byte units.
+        // dS^T over the next 16 columns, and row r of the swizzled dS^T tile
+        // (queries cbase .. cbase+31: four 16-byte units).
+        tmem_st16(tS + 16, dk);
         uint8_t* ds_row = smem_raw + Ly::DS_OFF + hc * Ly::CHUNK + r * 128;
 #pragma unroll
         for (int v = 0; v < 4; ++v) {
@@ -476,14 +513,15 @@ __global__ void __launch_bounds__(512, 1)
         fence_proxy_async_smem();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(bar(Ly::B_PFULL + hc));
+        if (lane == 0) mbar_arrive(bar(Ly::B_DSFULL + hc));
       }
+      if (!ok) break;
       if (++stage == Ly::STAGES) stage = 0;
     }
     const int hc = sub;  // epilogue role: warps 0-3 write dK, warps 4-7 write dV
     // Epilogue: warpgroup A writes dK (scaled by 1/sqrt(D)), B writes dV.
     if (!ok) break;
-    if (!mbar_wait_warp(bar(Ly::B_DKVFULL), kv_cnt & 1, ab, err, 602)) { ok = false; break; }
+    if (!mbar_wait_warp(bar(Ly::B_DKVFULL), kv_cnt & 1, ab, err, 603)) { ok = false; break; }
     {
       tc_fence_after();
       void* dst_base = hc == 0 ? p.dK : p.dV;
@@ -511,6 +549,7 @@ __global__ void __launch_bounds__(512, 1)
     ++kv_cnt;
     }
   } else if (warp < 12) {
+    if constexpr (kSplitRegs) setmaxnreg_inc<176>();
     // ------------------------------------------------------------ dQ drain
     const int r = threadIdx.x & 127;  // query row within the Q tile == TMEM lane
     const uint32_t lane_off = ((warp & 3u) * 32u) << 16;
@@ -531,39 +570,39 @@ __global__ void __launch_bounds__(512, 1)
       // 4-column group are 512 contiguous bytes.
       float4* acc = reinterpret_cast<float4*>(p.dq_accum) +
                     (static_cast<size_t>(it.b) * p.H + h) * (D / 4) * p.Lpad + q;
+      // The whole dQ row (D fp32) in registers, then its columns go back to
+      // the MMA warp before any reduction is issued.
+      uint32_t gq[D];
 #pragma unroll
-      for (int hq = 0; hq < Ly::NDQ; ++hq) {
-        uint32_t gq[64];
-        tmem_ld32(tmem + lane_off + Ly::tm_dq(hq), gq);
-        tmem_ld32(tmem + lane_off + Ly::tm_dq(hq) + 32, gq + 32);
-        tmem_ld_wait32(gq);
-        tmem_ld_wait32(gq + 32);
-        // This half is in registers: release its columns before the atomics.
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar(Ly::B_DQEMPTY + hq));
-        if (q < p.Lq) {
+      for (int cc = 0; cc < D / 32; ++cc) tmem_ld32(tmem + lane_off + Ly::TM_DP + 32 * cc, gq + 32 * cc);
 #pragma unroll
-          for (int c4 = 0; c4 < 16; ++c4) {
-            // Pace the second half's reductions (D = 128 only): issued back
-            // to back they overlap the first query half of the next tile and
-            // slow its compute warps.  Measured at B8 H32 L4096 D128: 5.54 ms
-            // unpaced, 5.15 ms with four 512 ns pauses, which is 0.7 of the
-            // ~2.9 us a 128 x 128 tile takes at 2.07 GHz (lower clocks only
-            // lengthen the tile).  __nanosleep(t) sleeps for the power of two
-            // above t (300-500 -> 512 ns); four pauses of 1,024 ns outlast a
-            // tile and the drain falls behind (7.4 ms); pausing the first half
-            // instead is slower.  A late drain only delays the MMA warp's
-            // bounded wait on the dQ-empty barrier.
-            if (hq == 1 && (c4 & 3) == 3) __nanosleep(384);
-            red_add_v4(reinterpret_cast<float*>(acc + static_cast<size_t>(16 * hq + c4) * p.Lpad),
-                       __uint_as_float(gq[4 * c4]), __uint_as_float(gq[4 * c4 + 1]),
-                       __uint_as_float(gq[4 * c4 + 2]), __uint_as_float(gq[4 * c4 + 3]));
-          }
+      for (int cc = 0; cc < D / 32; ++cc) tmem_ld_wait32(gq + 32 * cc);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(Ly::B_DQEMPTY));
+      if (q < p.Lq) {
+#pragma unroll
+        for (int c4 = 0; c4 < D / 4; ++c4) {
+          // Paced: issued back to back, a tile's reductions hold the SM's
+          // memory-instruction path for ~1,000 cycles and slow the MMAs that
+          // read shared memory meanwhile (the next tile's S^T and dP^T).  At
+          // B8 H32 L4096 D128 (a tile every ~2.6 us): 5.60 ms unpaced, 4.48 ms
+          // with a 64 ns pause after each reduction (31 pauses, ~2 us);
+          // bursts of more than four, or pauses adding up to the tile time,
+          // are slower.  __nanosleep(t) sleeps for the power of two above t.
+          if ((D == 128 || FA_BWD_PACE_D64) && FA_BWD_PACE_NS > 0 &&
+              (c4 % FA_BWD_PACE_EVERY) == FA_BWD_PACE_EVERY - 1 && c4 < D / 4 - 1)
+            __nanosleep(FA_BWD_PACE_NS);
+          red_add_v4(reinterpret_cast<float*>(acc + static_cast<size_t>(c4) * p.Lpad),
+                     __uint_as_float(gq[4 * c4]), __uint_as_float(gq[4 * c4 + 1]),
+                     __uint_as_float(gq[4 * c4 + 2]), __uint_as_float(gq[4 * c4 + 3]));
         }
       }
     }
     }
+  } else {
+    // warps 14-15: idle, but they belong to the producer / MMA warpgroup
+    if constexpr (kSplitRegs) setmaxnreg_dec<80>();
   }
 
   tc_fence_before();

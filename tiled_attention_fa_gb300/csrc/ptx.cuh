@@ -366,6 +366,19 @@ __device__ __forceinline__ void tmem_ld_wait16(uint32_t* r) {
 }
 
 // Store 16 consecutive columns of this thread's lane.
+// Per-warpgroup register budget (every warp of the warpgroup executes the
+// same instruction).  An increase waits until decreases elsewhere in the CTA
+// have returned enough of the registers the CTA was launched with, so the
+// budgets of all warpgroups must sum to at most that launch total.
+template <uint32_t N>
+__device__ __forceinline__ void setmaxnreg_inc() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <uint32_t N>
+__device__ __forceinline__ void setmaxnreg_dec() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+
 __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t* r) {
   asm volatile(
       "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
