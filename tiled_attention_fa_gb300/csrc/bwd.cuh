@@ -32,9 +32,10 @@
 // An MMA with both operands in shared memory reads them at the shared-memory
 // rate (128 B per clock: an M=128 N=128 K=16 step, 8 KB, takes its 64 tensor
 // cycles in reads alone), so the schedule keeps every operand it can in TMEM:
-// per tile S^T and dP^T (both operands in shared memory, N = 128 queries),
-// dV and dK (A from TMEM), dQ (both in shared memory): 40 MMAs, 256 KB of
-// operand reads.  dK and dV stay in TMEM for a whole K/V tile; for
+// per tile S^T and dP^T (both operands in shared memory, N = 128 queries;
+// at D = 64 K_j and V_j are copied into spare TMEM columns once per K/V tile
+// and these read only Q / dO), dV and dK (A from TMEM), dQ (both in shared
+// memory): 40 MMAs, 256 KB of operand reads at D = 128.  dK and dV stay in TMEM for a whole K/V tile; for
 // grouped-query attention the CTA loops over every query head of its K/V
 // head, so dK/dV need no atomics.
 #pragma once
@@ -109,6 +110,11 @@ struct BwdLayout {
   // halves are consumed; the next tile's S^T never waits for the dQ drain,
   // only its dP^T does.
   static constexpr uint32_t TM_DK = 0, TM_DV = D, TM_S = 2 * D, TM_DP = 2 * D + 128;
+  // At D = 64 K_j and V_j also live in TMEM (32 columns of 16-bit pairs each),
+  // copied there once per K/V tile, so S^T and dP^T read only Q / dO from
+  // shared memory (at D = 128 the columns are all taken).
+  static constexpr bool KV_TMEM = (D == 64);
+  static constexpr uint32_t TM_K = 2 * D + 256, TM_V = TM_K + D / 2;
   static constexpr uint32_t TMEM_COLS = 512;
   static constexpr int NTHREADS = 512;
 };
@@ -322,6 +328,18 @@ __global__ void __launch_bounds__(512, 1)
     const BwdItem it = bwd_decode(item, p);
     if (!mbar_wait_warp(bar(Ly::B_KVFULL), kv_cnt & 1, ab, err, 501)) { ok = false; break; }
     tc_fence_after();
+    if constexpr (Ly::KV_TMEM) {
+      // K_j, V_j into TMEM, one 16-column K step per copy (after the previous
+      // item's MMAs that read these columns, which were issued before).
+      if (elect_one()) {
+#pragma unroll
+        for (int k = 0; k < D / 16; ++k) {
+          tmem_cp_128x256b(tmem + Ly::TM_K + 8 * k, kd + koff(k));
+          tmem_cp_128x256b(tmem + Ly::TM_V + 8 * k, vd + koff(k));
+        }
+      }
+      __syncwarp();
+    }
     // n: tile within the item (accumulate flags); g: tile of the CTA (phases)
     for (int n = 0; ok && n < it.ntiles; ++n, ++g) {
       if (!mbar_wait_warp(bar(Ly::B_QFULL + stage), phase, ab, err, 502)) { ok = false; break; }
@@ -335,7 +353,10 @@ __global__ void __launch_bounds__(512, 1)
       if (elect_one()) {
 #pragma unroll
         for (int k = 0; k < D / 16; ++k)
-          mma_ss(tmem + Ly::TM_S, kd + koff(k), qd + koff(k), IDESC_S, k > 0 ? 1u : 0u);
+          if constexpr (Ly::KV_TMEM)
+            mma_ts(tmem + Ly::TM_S, tmem + Ly::TM_K + 8 * k, qd + koff(k), IDESC_S, k > 0 ? 1u : 0u);
+          else
+            mma_ss(tmem + Ly::TM_S, kd + koff(k), qd + koff(k), IDESC_S, k > 0 ? 1u : 0u);
         tc_commit(bar(Ly::B_SFULL));
       }
       __syncwarp();
@@ -348,7 +369,10 @@ __global__ void __launch_bounds__(512, 1)
       if (elect_one()) {
 #pragma unroll
         for (int k = 0; k < D / 16; ++k)
-          mma_ss(tmem + Ly::TM_DP, vd + koff(k), dod + koff(k), IDESC_S, k > 0 ? 1u : 0u);
+          if constexpr (Ly::KV_TMEM)
+            mma_ts(tmem + Ly::TM_DP, tmem + Ly::TM_V + 8 * k, dod + koff(k), IDESC_S, k > 0 ? 1u : 0u);
+          else
+            mma_ss(tmem + Ly::TM_DP, vd + koff(k), dod + koff(k), IDESC_S, k > 0 ? 1u : 0u);
         tc_commit(bar(Ly::B_DPFULL));
       }
       __syncwarp();

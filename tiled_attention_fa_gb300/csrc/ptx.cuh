@@ -196,6 +196,14 @@ __device__ __forceinline__ void tc_commit(uint32_t bar) {
                : "memory");
 }
 
+// Asynchronous copy of 128 rows x 32 bytes from shared memory (laid out as
+// the matrix descriptor says, the same form an MMA's A operand read takes)
+// into TMEM: row i lands in lane i, columns taddr .. taddr+7.  Ordered with the
+// issuing thread's MMAs and tracked by its commits like them.
+__device__ __forceinline__ void tmem_cp_128x256b(uint32_t taddr, uint64_t sdesc) {
+  asm volatile("tcgen05.cp.cta_group::1.128x256b [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
+}
+
 // True in exactly one lane of a converged warp (the same lane every time the
 // whole warp executes it).  MMAs and the commits that track them are issued
 // under it, so the operands stay warp-uniform values.
