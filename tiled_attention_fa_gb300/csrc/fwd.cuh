@@ -72,6 +72,11 @@ struct FwdLayout {
   static constexpr uint32_t SMEM_USED = MISC_OFF + 16;
   static constexpr uint32_t SMEM_ALLOC = SMEM_USED + 1024;  // slack for 1024-byte alignment
   static constexpr uint32_t TM_S0 = 0, TM_S1 = 128, TM_O0 = 256, TM_O1 = 256 + D;
+  // At D = 64 (16-bit inputs) the Q tiles also live in TMEM (32 columns of
+  // 16-bit pairs each), copied there once per item, so S = Q K^T reads only
+  // K from shared memory.
+  static constexpr bool Q_TMEM = (D == 64 && !FP8);
+  static constexpr uint32_t TM_Q0 = 256 + 2 * D, TM_Q1 = TM_Q0 + D / 2;
   static constexpr uint32_t TMEM_COLS = 512;
   static constexpr int NTHREADS = 320;
 };
@@ -260,6 +265,9 @@ __global__ void __launch_bounds__(320, 1)
             const uint64_t off = ((k >> 2) * Ly::CHUNK + (k & 3) * 32u) >> 4;
             if constexpr (FP8)
               mma_ss_f8(tS(t), qd + off, kd + off, IDESC_S, k > 0 ? 1u : 0u);
+            else if constexpr (Ly::Q_TMEM)
+              mma_ts(tS(t), tmem + (t ? Ly::TM_Q1 : Ly::TM_Q0) + 8u * k, kd + off, IDESC_S,
+                     k > 0 ? 1u : 0u);
             else
               mma_ss(tS(t), qd + off, kd + off, IDESC_S, k > 0 ? 1u : 0u);
           }
@@ -300,6 +308,21 @@ __global__ void __launch_bounds__(320, 1)
         if (!mbar_wait_warp(bar(Ly::B_QFULL), q_cnt & 1, ab, err, 201)) { ok = false; break; }
         ++q_cnt;
         tc_fence_after();
+        if constexpr (Ly::Q_TMEM) {
+          // Both Q tiles into TMEM (after the previous item's S MMAs, which
+          // read these columns and were issued before).
+          if (elect_one()) {
+#pragma unroll
+            for (int t = 0; t < 2; ++t) {
+              const uint64_t qd = sdesc_sw128(base + Ly::Q_OFF + t * Ly::TILE, 16, 1024);
+#pragma unroll
+              for (int k = 0; k < Ly::KS_S; ++k)
+                tmem_cp_128x256b(tmem + (t ? Ly::TM_Q1 : Ly::TM_Q0) + 8u * k,
+                                 qd + (((k >> 2) * Ly::CHUNK + (k & 3) * 32u) >> 4));
+            }
+          }
+          __syncwarp();
+        }
         // Pair 0 holds K_0: the first S of both tiles.
         uint32_t ps;
         if (!take(ps, 202)) { ok = false; break; }
