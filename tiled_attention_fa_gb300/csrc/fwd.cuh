@@ -322,6 +322,9 @@ __global__ void __launch_bounds__(320, 1)
             }
           }
           __syncwarp();
+          // The copies are the only readers of the Q tiles in shared memory:
+          // the next item's Q may load as soon as they complete.
+          commit(Ly::B_QEMPTY);
         }
         // Pair 0 holds K_0: the first S of both tiles.
         uint32_t ps;
@@ -367,7 +370,7 @@ __global__ void __launch_bounds__(320, 1)
           commit(Ly::B_KVEMPTY + ps);
         }
         if (!ok) break;
-        commit(Ly::B_QEMPTY);
+        if constexpr (!Ly::Q_TMEM) commit(Ly::B_QEMPTY);
       }
       // Every MMA issued by the elected lane completes before TMEM is released.
       commit(Ly::B_DONE);
