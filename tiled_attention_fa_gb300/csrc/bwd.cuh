@@ -24,8 +24,9 @@
 //   warps 8-11 dQ drain: thread r owns query row r; takes the whole dQ row
 //              from TMEM, releases the columns, then adds it into the fp32
 //              accumulator with paced 16-byte vector reductions.
-//   warp  12   TMA producer: K_j, V_j once per K/V tile; then Q_i, dO_i (and
-//              LSE_i, Delta_i) through a two-slot ring.
+//   warp  12   TMA producer: K_j, V_j once per K/V tile (two slots at D = 64,
+//              so the next tile's load overlaps the current one); then Q_i,
+//              dO_i (and LSE_i, Delta_i) through a two-slot ring.
 //   warp  13   TMEM allocator and MMA issuer (the warp runs the schedule,
 //              one elected lane issues the MMAs and their commits).
 //   warps 14-15 idle (they only lower their register budget with 12-13).
@@ -85,21 +86,26 @@ struct BwdLayout {
   static constexpr uint32_t CHUNK = 128u * 128u;
   static constexpr uint32_t TILE = KCH * CHUNK;
   static constexpr int STAGES = 2;
+  // K/V slots: at D = 64 shared memory has room for a second (K, V) pair, so
+  // the next K/V tile loads while the current one is in use.
+  static constexpr int KVS = (D == 64) ? 2 : 1;
   // Small region first (barriers, TMEM address, abort flag, LSE/Delta slots),
   // then the 1024-byte aligned operand tiles.
-  static constexpr int B_KVFULL = 0, B_QFULL = 1, B_QEMPTY = 1 + STAGES, B_SFULL = 1 + 2 * STAGES,
+  static constexpr int B_KVFULL = 0, B_QFULL = KVS, B_QEMPTY = KVS + STAGES,
+                       B_SFULL = KVS + 2 * STAGES,
                        B_DPFULL = B_SFULL + 1, B_PFULL = B_DPFULL + 1, B_DSFULL = B_PFULL + 2,
                        B_DQFULL = B_DSFULL + 2, B_DQEMPTY = B_DQFULL + 1,
                        B_DKVFULL = B_DQEMPTY + 1, B_DONE = B_DKVFULL + 1, B_KVEMPTY = B_DONE + 1,
-                       NBAR = B_KVEMPTY + 1;
+                       NBAR = B_KVEMPTY + KVS;
   static constexpr uint32_t BAR_OFF = 0;
   static constexpr uint32_t MISC_OFF = BAR_OFF + NBAR * 8;              // tmem slot, abort flag
   static constexpr uint32_t STAT_OFF = (MISC_OFF + 16 + 15) / 16 * 16;  // [STAGES][2][128] f32
   static constexpr uint32_t SMALL_END = STAT_OFF + STAGES * 2 * 128 * 4;
   static constexpr uint32_t TILE_BASE = (SMALL_END + 1023) / 1024 * 1024;
-  static constexpr uint32_t K_OFF = TILE_BASE;
-  static constexpr uint32_t V_OFF = K_OFF + TILE;
-  static constexpr uint32_t Q_OFF = V_OFF + TILE;             // [STAGES] tiles
+  static constexpr uint32_t KV_OFF = TILE_BASE;                 // [KVS] (K, V) tile pairs
+  __host__ __device__ static constexpr uint32_t k_off(int slot) { return KV_OFF + 2u * slot * TILE; }
+  __host__ __device__ static constexpr uint32_t v_off(int slot) { return k_off(slot) + TILE; }
+  static constexpr uint32_t Q_OFF = KV_OFF + 2 * KVS * TILE;   // [STAGES] tiles
   static constexpr uint32_t DO_OFF = Q_OFF + STAGES * TILE;   // [STAGES] tiles
   static constexpr uint32_t DS_OFF = DO_OFF + STAGES * TILE;  // 2 chunks (128 keys x 128 queries)
   static constexpr uint32_t SMEM_ALLOC = DS_OFF + 2 * CHUNK;
@@ -194,8 +200,10 @@ __global__ void __launch_bounds__(512, 1)
     return;
   }
   if (threadIdx.x == 0) {
-    mbar_init(bar(Ly::B_KVFULL), 1);
-    mbar_init(bar(Ly::B_KVEMPTY), 1);
+    for (int s = 0; s < Ly::KVS; ++s) {
+      mbar_init(bar(Ly::B_KVFULL + s), 1);
+      mbar_init(bar(Ly::B_KVEMPTY + s), 1);
+    }
     for (int s = 0; s < Ly::STAGES; ++s) {
       mbar_init(bar(Ly::B_QFULL + s), 1);
       mbar_init(bar(Ly::B_QEMPTY + s), 1);
@@ -252,16 +260,19 @@ __global__ void __launch_bounds__(512, 1)
     int item;
     if (!bwd_unit_item(u / p.ipu, u % p.ipu, p, item)) continue;
     const BwdItem it = bwd_decode(item, p);
-    if (kv_cnt > 0 && !mbar_wait_warp(bar(Ly::B_KVEMPTY), (kv_cnt - 1) & 1, ab, err, 402)) {
+    const int kvs = static_cast<int>(kv_cnt % Ly::KVS);
+    const uint32_t kv_round = kv_cnt / Ly::KVS;
+    if (kv_round > 0 &&
+        !mbar_wait_warp(bar(Ly::B_KVEMPTY + kvs), (kv_round - 1) & 1, ab, err, 402)) {
       ok = false;
       break;
     }
     if (lane == 0) {
-      mbar_arrive_expect_tx(bar(Ly::B_KVFULL), 2 * Ly::TILE);
+      mbar_arrive_expect_tx(bar(Ly::B_KVFULL + kvs), 2 * Ly::TILE);
       for (int c = 0; c < Ly::KCH; ++c) {
-        tma_load_4d(base + Ly::K_OFF + c * Ly::CHUNK, &tmK, bar(Ly::B_KVFULL), c * 64, it.hkv,
+        tma_load_4d(base + Ly::k_off(kvs) + c * Ly::CHUNK, &tmK, bar(Ly::B_KVFULL + kvs), c * 64, it.hkv,
                     it.j * 128, it.b);
-        tma_load_4d(base + Ly::V_OFF + c * Ly::CHUNK, &tmV, bar(Ly::B_KVFULL), c * 64, it.hkv,
+        tma_load_4d(base + Ly::v_off(kvs) + c * Ly::CHUNK, &tmV, bar(Ly::B_KVFULL + kvs), c * 64, it.hkv,
                     it.j * 128, it.b);
       }
     }
@@ -299,7 +310,8 @@ __global__ void __launch_bounds__(512, 1)
     }
     }
     if (!ok && lane == 0) {
-      if (kv_cnt > 0) mbar_wait_drain(bar(Ly::B_KVFULL), (kv_cnt - 1) & 1);
+      for (uint32_t c = kv_cnt > Ly::KVS ? kv_cnt - Ly::KVS : 0; c < kv_cnt; ++c)
+        mbar_wait_drain(bar(Ly::B_KVFULL + c % Ly::KVS), (c / Ly::KVS) & 1);
       for (int s = 0; s < Ly::STAGES; ++s)
         if (issued[s] > 0) mbar_wait_drain(bar(Ly::B_QFULL + s), (issued[s] - 1) & 1);
     }
@@ -316,9 +328,7 @@ __global__ void __launch_bounds__(512, 1)
     uint32_t stage = 0, phase = 0, g = 0, kv_cnt = 0;
     // Descriptors of the first K step (K-major operands) or of the first 16
     // rows (MN-major); later steps add their byte offset >> 4.
-    const uint64_t kd = sdesc_sw128(base + Ly::K_OFF, 16, 1024);
-    const uint64_t vd = sdesc_sw128(base + Ly::V_OFF, 16, 1024);
-    const uint64_t kd_mn = sdesc_sw128(base + Ly::K_OFF, Ly::CHUNK, 1024);
+    uint64_t kd = 0, vd = 0, kd_mn = 0;  // the current K/V slot's (set per item)
     const uint64_t dsd_mn = sdesc_sw128(base + Ly::DS_OFF, Ly::CHUNK, 1024);
     auto koff = [](int k) -> uint64_t { return ((k >> 2) * Ly::CHUNK + (k & 3) * 32u) >> 4; };
     for (int u = p.ipu * static_cast<int>(blockIdx.x); ok && u < p.ipu * p.n_units;
@@ -326,8 +336,15 @@ __global__ void __launch_bounds__(512, 1)
     int item;
     if (!bwd_unit_item(u / p.ipu, u % p.ipu, p, item)) continue;
     const BwdItem it = bwd_decode(item, p);
-    if (!mbar_wait_warp(bar(Ly::B_KVFULL), kv_cnt & 1, ab, err, 501)) { ok = false; break; }
+    const int kvs = static_cast<int>(kv_cnt % Ly::KVS);
+    if (!mbar_wait_warp(bar(Ly::B_KVFULL + kvs), (kv_cnt / Ly::KVS) & 1, ab, err, 501)) {
+      ok = false;
+      break;
+    }
     tc_fence_after();
+    kd = sdesc_sw128(base + Ly::k_off(kvs), 16, 1024);
+    vd = sdesc_sw128(base + Ly::v_off(kvs), 16, 1024);
+    kd_mn = sdesc_sw128(base + Ly::k_off(kvs), Ly::CHUNK, 1024);
     if constexpr (Ly::KV_TMEM) {
       // K_j, V_j into TMEM, one 16-column K step per copy (after the previous
       // item's MMAs that read these columns, which were issued before).
@@ -422,7 +439,7 @@ __global__ void __launch_bounds__(512, 1)
     // dK / dV of this item are final; K_j / V_j are no longer read.
     if (elect_one()) {
       tc_commit(bar(Ly::B_DKVFULL));
-      tc_commit(bar(Ly::B_KVEMPTY));
+      tc_commit(bar(Ly::B_KVEMPTY + kvs));
     }
     __syncwarp();
     ++kv_cnt;
