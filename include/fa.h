@@ -32,7 +32,11 @@ extern "C" {
 typedef enum {
   FA_OK = 0,
   FA_ERR_INVALID_ARG = 1,    /* null/misaligned pointer, bad size, H % Hkv != 0 */
-  FA_ERR_UNSUPPORTED = 2,    /* D or dtype outside the supported set */
+  FA_ERR_UNSUPPORTED = 2,    /* D or dtype outside the supported set, or the device or the
+                                build cannot run the kernel as designed (too little shared
+                                memory per block; a backward kernel compiled with a register
+                                allocation other than its warpgroup split assumes);
+                                nothing was launched */
   FA_ERR_CUDA = 3,           /* a CUDA runtime call or kernel launch failed */
   FA_ERR_DEVICE_TIMEOUT = 4, /* a kernel gave up a bounded wait (see fa_check_device_error) */
   FA_ERR_SCRATCH_TOO_SMALL = 5 /* fa_bwd_noalloc's fixed scratch or fa_decode's workspace is

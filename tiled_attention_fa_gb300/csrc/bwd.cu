@@ -78,6 +78,20 @@ static fa_status launch_bwd(const void* Q, const void* K, const void* V, const v
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Ly::SMEM_ALLOC) !=
       cudaSuccess)
     return FA_ERR_CUDA;
+  if constexpr (D == 128) {
+    // The kernel moves 48 registers per thread from the producer / MMA
+    // warpgroup to the dQ drain warpgroup (setmaxnreg 80 / 176); that balances
+    // only when every thread starts with 128.  Any other allocation would
+    // leave the increase waiting for registers that never come back, so
+    // refuse to launch instead.
+    static int num_regs = -1;
+    static std::once_flag once;
+    std::call_once(once, [&] {
+      cudaFuncAttributes a;
+      if (cudaFuncGetAttributes(&a, kern) == cudaSuccess) num_regs = a.numRegs;
+    });
+    if (num_regs != Ly::NTHREADS_REGS) return FA_ERR_UNSUPPORTED;
+  }
   const int grid = p.n_units < sm_count() ? p.n_units : sm_count();  // persistent CTAs
   kern<<<grid, Ly::NTHREADS, Ly::SMEM_ALLOC, s>>>(tq, tk, tv, tdo, p);
   return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;

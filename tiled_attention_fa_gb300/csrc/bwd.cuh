@@ -15,8 +15,8 @@
 //   warps 0-7  compute warps: each query half of a tile (columns 0-63, then
 //              64-127) is split over all eight, warp w taking 32 columns
 //              of key rows 32*(w%4).. (its TMEM lanes); a thread owns one
-//              key row and forms
-//              P^T = exp2(S^T*c - LSE*log2e) and dS^T = P^T o (dP^T - Delta);
+//              key row and forms P^T = exp2(S^T*c - LSE*log2e) as soon as
+//              S^T lands, then dS^T = P^T o (dP^T - Delta) once dP^T does;
 //              both go back to TMEM over the chunk's S^T columns (A operands
 //              of dV += P^T dO and dK += dS^T Q) and dS^T also to a swizzled
 //              smem tile (read MN-major as the A operand of dQ = dS K).  At
@@ -36,9 +36,9 @@
 // per tile S^T and dP^T (both operands in shared memory, N = 128 queries;
 // at D = 64 K_j and V_j are copied into spare TMEM columns once per K/V tile
 // and these read only Q / dO), dV and dK (A from TMEM), dQ (both in shared
-// memory): 40 MMAs, 256 KB of operand reads at D = 128.  dK and dV stay in TMEM for a whole K/V tile; for
-// grouped-query attention the CTA loops over every query head of its K/V
-// head, so dK/dV need no atomics.
+// memory): 40 MMAs, 256 KB of operand reads at D = 128.  dK and dV stay in
+// TMEM for a whole K/V tile; for grouped-query attention the CTA loops over
+// every query head of its K/V head, so dK/dV need no atomics.
 #pragma once
 
 #include <cuda_bf16.h>
@@ -48,8 +48,9 @@
 #include "fwd.cuh"  // pack2
 #include "ptx.cuh"
 
-// Pacing of the dQ drain's reductions at D = 128: a pause of FA_BWD_PACE_NS
-// after every FA_BWD_PACE_EVERY reductions (see the drain).
+// Pacing of the dQ drain's reductions: a pause of FA_BWD_PACE_NS after every
+// FA_BWD_PACE_EVERY reductions at D = 128, and at D = 64 unless
+// FA_BWD_PACE_D64 is 0 (see the drain).
 #ifndef FA_BWD_PACE_NS
 #define FA_BWD_PACE_NS 50
 #endif
@@ -123,6 +124,9 @@ struct BwdLayout {
   static constexpr uint32_t TM_K = 2 * D + 256, TM_V = TM_K + D / 2;
   static constexpr uint32_t TMEM_COLS = 512;
   static constexpr int NTHREADS = 512;
+  // Registers per thread at launch (65,536 / NTHREADS); the D = 128 register
+  // split between warpgroups assumes exactly this many.
+  static constexpr int NTHREADS_REGS = 65536 / NTHREADS;
 };
 
 struct BwdItem {

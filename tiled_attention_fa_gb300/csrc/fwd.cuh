@@ -15,9 +15,10 @@
 //   warp  8    TMA producer: Q pair, then (V_{j-1}, K_j) tile pairs into a ring
 //   warp  9    TMEM allocator and MMA issuer (the warp runs the schedule,
 //              one elected lane issues the MMAs and their commits)
-// Registers are not re-balanced between warps (no setmaxnreg): a fixed split
-// depends on the launch allocation and would wait forever if a tool or
-// compiler changed it; the softmax instead stays within the uniform budget.
+// Registers are not re-balanced between warps (no setmaxnreg): the softmax
+// fits the uniform budget of 168 per thread.  (The backward does move
+// registers between warpgroups; its launcher checks the launch allocation the
+// split relies on.)
 // A work item is (batch, head, pair of 128-row Q tiles).  S_t = Q_t K_j^T and
 // O_t += P_t V_j accumulate in tensor memory; P_t overwrites S_t in TMEM as
 // 16-bit values and is read from there by the PV MMA.  While warpgroup 0
