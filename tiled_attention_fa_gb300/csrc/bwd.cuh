@@ -127,6 +127,12 @@ struct BwdLayout {
   // Registers per thread at launch (65,536 / NTHREADS); the D = 128 register
   // split between warpgroups assumes exactly this many.
   static constexpr int NTHREADS_REGS = 65536 / NTHREADS;
+  // The column plan and the shared-memory plan fit the hardware.
+  static_assert(TM_S >= TM_DV + D && TM_DP >= TM_S + 128 && TM_DP + 128 <= TMEM_COLS,
+                "TMEM regions overlap or overflow");
+  static_assert(!KV_TMEM || (TM_K >= TM_DP + 128 && TM_V + D / 2 <= TMEM_COLS),
+                "TMEM copies of K / V overlap or overflow");
+  static_assert(SMEM_ALLOC <= 232448, "shared memory beyond the 227 KB per-block limit");
 };
 
 struct BwdItem {

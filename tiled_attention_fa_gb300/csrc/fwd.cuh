@@ -79,6 +79,9 @@ struct FwdLayout {
   static constexpr bool Q_TMEM = (D == 64 && !FP8);
   static constexpr uint32_t TM_Q0 = 256 + 2 * D, TM_Q1 = TM_Q0 + D / 2;
   static constexpr uint32_t TMEM_COLS = 512;
+  static_assert(TM_O1 + D <= TMEM_COLS, "TMEM regions overflow");
+  static_assert(!Q_TMEM || TM_Q1 + D / 2 <= TMEM_COLS, "TMEM copies of Q overflow");
+  static_assert(SMEM_ALLOC <= 232448, "shared memory beyond the 227 KB per-block limit");
   static constexpr int NTHREADS = 320;
 };
 
