@@ -52,10 +52,10 @@
 // FA_BWD_PACE_EVERY reductions at D = 128, and at D = 64 unless
 // FA_BWD_PACE_D64 is 0 (see the drain).
 #ifndef FA_BWD_PACE_NS
-#define FA_BWD_PACE_NS 50
+#define FA_BWD_PACE_NS 100
 #endif
 #ifndef FA_BWD_PACE_EVERY
-#define FA_BWD_PACE_EVERY 1
+#define FA_BWD_PACE_EVERY 2
 #endif
 #ifndef FA_BWD_PACE_D64
 #define FA_BWD_PACE_D64 1
@@ -642,10 +642,12 @@ __global__ void __launch_bounds__(512, 1)
           // Paced: issued back to back, a tile's reductions hold the SM's
           // memory-instruction path for ~1,000 cycles and slow the MMAs that
           // read shared memory meanwhile (the next tile's S^T and dP^T).  At
-          // B8 H32 L4096 D128 (a tile every ~2.6 us): 5.60 ms unpaced, 4.48 ms
-          // with a 64 ns pause after each reduction (31 pauses, ~2 us);
-          // bursts of more than four, or pauses adding up to the tile time,
-          // are slower.  __nanosleep(t) sleeps for the power of two above t.
+          // B8 H32 L4096 D128 (a tile every ~2.5 us): a 128 ns pause after
+          // every second reduction (15 pauses, ~1.9 us) 4.15 ms; 64 ns after
+          // each 4.24; 32 ns after each 4.66; 64 ns after every second 4.96;
+          // unpaced 5.60 on an earlier build.  Bursts of more than four, or
+          // pauses adding up to the tile time, are slower.  __nanosleep(t)
+          // sleeps for the power of two above t.
           if ((D == 128 || FA_BWD_PACE_D64) && FA_BWD_PACE_NS > 0 &&
               (c4 % FA_BWD_PACE_EVERY) == FA_BWD_PACE_EVERY - 1 && c4 < D / 4 - 1)
             __nanosleep(FA_BWD_PACE_NS);
