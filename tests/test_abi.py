@@ -2,7 +2,6 @@
 exports every function include/fa.h declares, and argument validation rejects
 bad calls before anything reaches the device."""
 
-import ctypes
 import os
 
 import pytest

@@ -6,7 +6,6 @@ the kernels' outputs for those units are compared element by element.  On all
 heads, the backward outputs are also checked against invariants that hold at
 any size: sum_j dV_j = sum_i dO_i and sum_j dK_j = 0 per (batch, kv-head)."""
 
-import numpy as np
 import pytest
 import torch
 
