@@ -60,6 +60,9 @@ WORKLOADS = {
                                            dtype="bf16"),
 }
 METRIC = "attention fwd/bwd TFLOP/s (fp16 B8 H32 L4096 D128) and % of GB300 TC peak"
+# Dense FP16/BF16 tensor rate per GPU from NVIDIA's published HGX B300 figures
+# (36 PFLOP/s per 8 GPUs with 2:4 sparsity, i.e. 2.25 PFLOP/s dense per GPU).
+DATASHEET_FP16_TFLOPS = 2250.0
 DECODE_METRIC = "attention split-KV decode GB/s (Q, K, V read + O, LSE written)"
 FP8_METRIC = "attention forward on E4M3 inputs TFLOP/s (4*B*H*L^2*D, halved causal)"
 _CSRC = "tiled_attention_fa_gb300/csrc/"
@@ -234,6 +237,29 @@ def time_oracle_units(q, k, v, do, causal, n_units, budget_s):
     return done, time.perf_counter() - t0
 
 
+def time_oracle_workload(causal, budget_s):
+    """Time the oracle's forward+backward over every (b, h) unit of the whole
+    workload when one unit's time says that fits in ``budget_s``; returns
+    (seconds, units) or None when it would not fit."""
+    from oracle import fa_oracle as orc
+    from tiled_attention_fa_gb300.inputs import make_qkv
+    B, L, H, Hkv, D = WORK["B"], WORK["L"], WORK["H"], WORK["Hkv"], WORK["D"]
+    if WORK.get("Lk", L) != L:
+        return None
+    q1, k1, v1, do1 = cpu_unit_inputs()
+    t0 = time.perf_counter()
+    orc.unit_backward(q1[0, :, 0], k1[0, :, 0], v1[0, :, 0], do1[0, :, 0], causal)
+    if (time.perf_counter() - t0) * B * H > budget_s:
+        return None
+    q, k, v, do = (t.double().numpy() for t in make_qkv(B, L, H, Hkv, D, WORK["dtype"], seed=0))
+    t0 = time.perf_counter()
+    for b in range(B):
+        for h in range(H):
+            hk = orc.kv_head(h, H, Hkv)
+            orc.unit_backward(q[b, :, h], k[b, :, hk], v[b, :, hk], do[b, :, h], causal)
+    return time.perf_counter() - t0, B * H
+
+
 def cpu_unit_inputs(seed=0):
     """One (b, h) unit of the workload, [1, L, 1, D] float64 host arrays (same recipe as the tests)."""
     from tiled_attention_fa_gb300.inputs import make_qkv
@@ -388,15 +414,22 @@ def ours_arm(args):
     for n in names:  # spread over the timed steps (the mean is "ms")
         kernels[n]["ms_median"] = statistics.median(per[n])
         kernels[n]["ms_min"] = min(per[n])
-    kernels["fa_fwd_kernel"]["frac_of_sustained"] = kernels["fa_fwd_kernel"]["tflops"] / sustained
-    kernels["fa_bwd_kernel"]["frac_of_sustained"] = kernels["fa_bwd_kernel"]["tflops"] / sustained
+    for n in ("fa_fwd_kernel", "fa_bwd_kernel"):
+        kernels[n]["frac_of_burst"] = kernels[n]["tflops"] / burst
+        kernels[n]["frac_of_sustained"] = kernels[n]["tflops"] / sustained
+        kernels[n]["frac_of_datasheet"] = kernels[n]["tflops"] / DATASHEET_FP16_TFLOPS
     dom = max(names, key=lambda n: kms[n])
     if dom in ("fa_fwd_kernel", "fa_bwd_kernel"):
+        # The kernels run for milliseconds inside a sub-second timed region: the
+        # burst figure (a GEMM timed alone) is the matching peak; the
+        # sustained figure (seconds back to back, under the power cap) and the
+        # datasheet's dense rate are reported beside it.
         ach = kernels[dom]["tflops"]
-        roof = {"kernel": dom, "bound": "tensor", "achieved": ach, "peak": sustained,
-                "unit": "TFLOP/s", "frac": ach / sustained,
-                "peak_source": f"{src} bf16 sustained (fp16 dense rate equals bf16)",
-                "frac_of_burst": ach / burst}
+        roof = {"kernel": dom, "bound": "tensor", "achieved": ach, "peak": burst,
+                "unit": "TFLOP/s", "frac": ach / burst,
+                "peak_source": f"{src} bf16 burst (fp16 dense rate equals bf16)",
+                "frac_of_sustained": ach / sustained,
+                "frac_of_datasheet": ach / DATASHEET_FP16_TFLOPS}
     else:
         ach = kernels[dom]["gbs"]
         roof = {"kernel": dom, "bound": "hbm", "achieved": ach, "peak": hbm, "unit": "GB/s",
@@ -434,12 +467,20 @@ def ours_arm(args):
     # ---- oracle on the host cores (rank 0, one GPU only)
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        uq, uk, uv, udo = cpu_unit_inputs()
-        n, secs = time_oracle_units(uq, uk, uv, udo, causal, 100000, args.cpu_budget)
-        cpu = {"value": n * step_flops(1, 1, L, D, causal) / secs / 1e12, "unit": "TFLOP/s",
-               "cores": blas_threads(), "kind": "oracle",
-               "sample": f"{n} (batch, head) unit(s) of the workload, forward+backward in fp64 "
-                         f"({secs:.1f} s)"}
+        full = time_oracle_workload(causal, 3 * args.cpu_budget)
+        if full is not None:
+            secs, n = full
+            cpu = {"value": step_flops(B, H, L, D, causal) / secs / 1e12, "unit": "TFLOP/s",
+                   "cores": blas_threads(), "kind": "oracle",
+                   "sample": f"the whole workload: all {n} (batch, head) units, forward+backward "
+                             f"in fp64 ({secs:.1f} s)"}
+        else:
+            uq, uk, uv, udo = cpu_unit_inputs()
+            n, secs = time_oracle_units(uq, uk, uv, udo, causal, 100000, args.cpu_budget)
+            cpu = {"value": n * step_flops(1, 1, L, D, causal) / secs / 1e12, "unit": "TFLOP/s",
+                   "cores": blas_threads(), "kind": "oracle",
+                   "sample": f"{n} (batch, head) unit(s) of the workload, forward+backward in "
+                             f"fp64 ({secs:.1f} s)"}
 
     if rank == 0:
         out = {
@@ -448,7 +489,7 @@ def ours_arm(args):
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": WORK["dtype"],
             "data": "synthetic", "config": config_dict(args, world),
             "frac_of_peak": {"burst": value / world / burst, "sustained": value / world / sustained,
-                             "source": src},
+                             "datasheet": value / world / DATASHEET_FP16_TFLOPS, "source": src},
             "step_stats": {"ms_mean": statistics.mean(step_ms), "ms_median": statistics.median(step_ms),
                            "ms_min": min(step_ms), "ms_max": max(step_ms),
                            "note": "this rank's per-step CUDA events; ms_per_step is the "

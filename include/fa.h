@@ -204,7 +204,9 @@ fa_status fa_bwd_postprocess(const float* dq_accum, void* dQ, int B, int L, int 
  * its own pool and hands out no allocator, or a serving path that must not
  * allocate once it has started.  This is a library facility; the pages have
  * no counterpart.
- * Same arguments and results as fa_bwd, minus the workspace: the fp32 dQ
+ * Same arguments and results as fa_bwd, minus the workspace.  Such a caller
+ * gets Delta from fa_bwd_preprocess with a NULL dq_accum (which needs no
+ * workspace either).  The fp32 dQ
  * accumulator lives in a fixed device array of FA_NOALLOC_SCRATCH_BYTES that
  * the library's module holds on every GPU that loads it, until exit.  The
  * call allocates nothing (no cudaMalloc, cudaFree or allocating library
@@ -216,9 +218,11 @@ fa_status fa_bwd_postprocess(const float* dq_accum, void* dQ, int B, int L, int 
  *   - Every call on a device shares the one array: calls whose work overlaps
  *     on the GPU (other streams, other host threads) race and corrupt each
  *     other's dQ.  Serialise them.
- *   - The first call on each device looks up the array's device address
- *     (with that device current); make that first call before any stream
- *     capture on the device.
+ *   - Each call looks up the array's device address on the current device
+ *     (the address can change if the device is reset and the module loaded
+ *     again) and remembers it; a call made while its stream is being
+ *     captured uses the remembered address instead.  Make the first call on
+ *     each device before any stream capture on that device.
  */
 #define FA_NOALLOC_SCRATCH_BYTES ((size_t)64 << 20)
 fa_status fa_bwd_noalloc(const void* Q, const void* K, const void* V, const void* O,

@@ -7,6 +7,8 @@ from .fa_oracle import (  # noqa: F401
     kv_head,
     storage_round,
     unit_backward,
+    unit_backward_parts,
     unit_forward,
+    unit_probs,
     unit_scores,
 )

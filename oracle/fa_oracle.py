@@ -65,11 +65,16 @@ softmax, no fusion):
   whose maximum lies in the first key tile they visit and otherwise only
   moves which way each value rounds.
 
-* The dK and dQ products: the pages print no cast of dS, but every GEMM in
-  their kernels multiplies tiles of the input type, and the backward casts
-  its transposed probabilities (the dV operand) to it.  Reading taken here:
-  dS is cast the same way before its two GEMMs; ``ds_round`` rounds dS to
-  that format for the dK and dQ products only (None = exact dS).
+* The dK and dQ products: the pages print no cast of dS, so the oracle
+  has none; its dS is exact.  (A kernel that multiplies a 16-bit dS on the
+  tensor cores differs from it by that rounding, which the tests bound.)
+
+* Intermediates for error bounds: ``unit_probs`` returns the probability
+  matrix of one unit together with exp(S - m) and its row sum, and
+  ``unit_backward_parts`` the matrices of the backward definition (P, dP,
+  Delta, dS, exact O).  They are the same arithmetic as ``unit_forward`` and
+  ``unit_backward``, exposed so that tests can bound a kernel's roundings
+  with exact values; nothing in them is specific to a kernel.
 
 * Backward (the page elides every step after the dV product): the analytic
   gradient of O = softmax(S) V,
@@ -112,6 +117,8 @@ __all__ = [
     "backward",
     "bwd_preprocess",
     "storage_round",
+    "unit_probs",
+    "unit_backward_parts",
     "e4m3_decode",
     "forward_fp8",
 ]
@@ -210,7 +217,7 @@ def unit_forward(q_bh, k_bh, v_bh, causal: bool, rows=None, panel: int = 4096, p
 
 
 def unit_backward(q_bh, k_bh, v_bh, do_bh, causal: bool, panel: int = 4096, o_round=None,
-                  p_round=None, ds_round=None, fwd_p_round=None):
+                  p_round=None, fwd_p_round=None):
     """Gradients of one (b, h) pair against its K/V head.
 
     q_bh, do_bh [Lq, D]; k_bh, v_bh [Lk, D] (Lq <= Lk under causal masking).
@@ -219,8 +226,7 @@ def unit_backward(q_bh, k_bh, v_bh, do_bh, causal: bool, panel: int = 4096, o_ro
     Formats (None, "fp16", "bf16"): ``o_round`` is the storage format of the
     O that Delta is formed from and ``fwd_p_round`` the forward's cast of
     exp(S - m) that made that O; ``p_round`` the format P is cast to for the
-    dV product; ``ds_round`` the format dS is cast to for the dK and dQ
-    products.  The returned O is the exact one.
+    dV product.  The returned O is the exact one.
     """
     q_bh, k_bh, v_bh, do_bh = (_as64(x) for x in (q_bh, k_bh, v_bh, do_bh))
     Lq, D = q_bh.shape
@@ -249,10 +255,36 @@ def unit_backward(q_bh, k_bh, v_bh, do_bh, causal: bool, panel: int = 4096, o_ro
         dv += storage_round(P, p_round).T @ dO  # dV = P^T dO (P cast for the product)
         dP = dO @ v_bh.T                        # dP = dO V^T
         dS = P * (dP - dl[:, None])             # dS = P o (dP - Delta)
-        dS = storage_round(dS, ds_round)        # (dS cast for its two products)
         dq[r] = (dS @ k_bh) * inv               # dQ = dS K / sqrt(D)
         dk += (dS.T @ q_bh[r]) * inv            # dK = dS^T Q / sqrt(D)
     return dq, dk, dv, delta, o, lse
+
+
+def unit_probs(q_bh, k_bh, causal: bool):
+    """Softmax parts of one (b, h): P [Lq, Lk] (rows sum to 1), E = exp(S - m)
+    with m the row max (so every row's largest entry is 1), and l [Lq], the
+    row sum of E (P = E / l).  Lq <= Lk under causal masking, bottom-right
+    aligned as in ``unit_forward``."""
+    q_bh, k_bh = _as64(q_bh), _as64(k_bh)
+    S = unit_scores(q_bh, k_bh, causal, 0, k_bh.shape[0] - q_bh.shape[0])
+    m = S.max(axis=1, keepdims=True)
+    E = np.exp(S - m)
+    l = E.sum(axis=1)
+    return E / l[:, None], E, l
+
+
+def unit_backward_parts(q_bh, k_bh, v_bh, do_bh, causal: bool):
+    """The matrices of the backward definition for one (b, h), all exact:
+    returns a dict with P [Lq, Lk], dP = dO V^T, Delta [Lq] (from the exact
+    O), dS = P o (dP - Delta 1^T) and O = P V.  dQ = dS K / sqrt(D) and
+    dK = dS^T Q / sqrt(D) follow from them as in ``unit_backward``."""
+    q_bh, k_bh, v_bh, do_bh = (_as64(x) for x in (q_bh, k_bh, v_bh, do_bh))
+    P, _, _ = unit_probs(q_bh, k_bh, causal)
+    O = P @ v_bh
+    dP = do_bh @ v_bh.T
+    delta = (O * do_bh).sum(axis=1)
+    dS = P * (dP - delta[:, None])
+    return {"P": P, "dP": dP, "Delta": delta, "dS": dS, "O": O}
 
 
 def forward(q, k, v, causal: bool, p_round=None):
@@ -280,8 +312,7 @@ def bwd_preprocess(o, do):
     return np.einsum("blhd,blhd->bhl", o, do)
 
 
-def backward(q, k, v, do, causal: bool, o_round=None, p_round=None, ds_round=None,
-             fwd_p_round=None):
+def backward(q, k, v, do, causal: bool, o_round=None, p_round=None, fwd_p_round=None):
     """Full backward over BSHD tensors.
 
     q, do [B, Lq, H, D]; k, v [B, Lk, Hkv, D].  Returns dQ [B, Lq, H, D],
@@ -300,7 +331,7 @@ def backward(q, k, v, do, causal: bool, o_round=None, p_round=None, ds_round=Non
             hk = kv_head(h, H, Hkv)
             gq, gk, gv, dl, _, _ = unit_backward(
                 q[b, :, h, :], k[b, :, hk, :], v[b, :, hk, :], do[b, :, h, :], causal,
-                o_round=o_round, p_round=p_round, ds_round=ds_round, fwd_p_round=fwd_p_round)
+                o_round=o_round, p_round=p_round, fwd_p_round=fwd_p_round)
             dq[b, :, h, :] = gq
             dk[b, :, hk, :] += gk                 # group heads sum into their KV head
             dv[b, :, hk, :] += gv

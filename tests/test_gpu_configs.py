@@ -1,47 +1,33 @@
 """Parity at the benchmark configurations' full sizes.
 
 The GPU runs each whole configuration through the same entry points the
-benchmark times; the oracle recomputes sampled (batch, head) units exactly and
-the kernels' outputs for those units are compared element by element.  On all
-heads, the backward outputs are also checked against invariants that hold at
-any size: sum_j dV_j = sum_i dO_i and sum_j dK_j = 0 per (batch, kv-head)."""
+benchmark times; the exact fp64 oracle recomputes (batch, head) units -- all
+of them where the host finishes them in well under a minute, otherwise a
+deterministic spread of at least eight -- on a pool of host processes, and
+the kernels' outputs for those units are compared element by element
+(O, dQ, dK, dV within 1e-2 + 1e-2 |ref|, LSE within 1e-3).  On all heads, the
+backward outputs are also checked against invariants that hold at any size:
+sum_j dV_j = sum_i dO_i and sum_j dK_j = 0 per (batch, kv-head)."""
 
 import pytest
 import torch
 
 import tiled_attention_fa_gb300 as fa
-from oracle import fa_oracle as orc
-from tests.helpers import LSE_ATOL, assert_close, kernel_casts
+from tests.oracle_pool import check_backward_units, check_forward_units
 from tiled_attention_fa_gb300.inputs import make_qkv
 
 pytestmark = pytest.mark.gpu
 
 
-def unit64(t, b, h):
-    return t[b, :, h].to(torch.float64).numpy()
+def all_units(B, H):
+    return [(b, h) for b in range(B) for h in range(H)]
 
 
-def check_fwd_units(q, k, v, o, lse, causal, units):
-    H, Hkv = q.shape[2], k.shape[2]
-    o, lse = o.cpu(), lse.cpu()
-    for b, h in units:
-        hk = orc.kv_head(h, H, Hkv)
-        ro, rl = orc.unit_forward(unit64(q, b, h), unit64(k, b, hk), unit64(v, b, hk), causal,
-                                  panel=2048)
-        assert_close(unit64(o, b, h), ro, name=f"O[{b},:,{h}]")
-        assert_close(lse[b, h].double().numpy(), rl, rtol=0, atol=LSE_ATOL, name=f"LSE[{b},{h}]")
-
-
-def check_bwd_units(q, k, v, do, dq, dk, dv, causal, units, dtype):
-    """MHA units: the K/V head of (b, h) receives gradient only from query head h."""
-    dq, dk, dv = dq.cpu(), dk.cpu(), dv.cpu()
-    for b, h in units:
-        rq, rk, rv, _, _, _ = orc.unit_backward(unit64(q, b, h), unit64(k, b, h), unit64(v, b, h),
-                                                unit64(do, b, h), causal, panel=2048,
-                                                **kernel_casts(dtype))
-        assert_close(unit64(dv, b, h), rv, name=f"dV[{b},:,{h}]")
-        assert_close(unit64(dk, b, h), rk, name=f"dK[{b},:,{h}]")
-        assert_close(unit64(dq, b, h), rq, name=f"dQ[{b},:,{h}]")
+def spread(B, H, n):
+    """n deterministic (b, h) units spread over the batch and the heads."""
+    total = B * H
+    idx = sorted({(i * total) // n + (i * 7) % max(1, total // n) for i in range(n)})
+    return [(i // H, i % H) for i in idx]
 
 
 def check_bwd_invariants(do, dk, dv, H, Hkv):
@@ -60,16 +46,17 @@ def check_bwd_invariants(do, dk, dv, H, Hkv):
 
 
 def run_fwd_bwd(q, k, v, do, causal, with_bwd=True):
+    """The whole configuration on the GPU; outputs back on the host."""
     qd, kd, vd = q.cuda(), k.cuda(), v.cuda()
     o, lse = fa.fwd(qd, kd, vd, causal)
     out = {"o": o, "lse": lse}
     if with_bwd:
         dod = do.cuda()
         dq, dk, dv, _ = fa.attention_backward(qd, kd, vd, o, lse, dod, causal)
-        out.update(dq=dq, dk=dk, dv=dv, do=dod)
+        out.update(dq=dq, dk=dk, dv=dv)
     torch.cuda.synchronize()
     fa.check_device_error()
-    return out
+    return {name: t.cpu() for name, t in out.items()}
 
 
 @pytest.fixture(scope="module")
@@ -82,35 +69,38 @@ def mha_b8_l4096():
 def test_mha_b8_h32_l4096_d128_fp16(cuda_lib, mha_b8_l4096, causal):
     q, k, v, do = mha_b8_l4096
     out = run_fwd_bwd(q, k, v, do, causal)
-    check_fwd_units(q, k, v, out["o"], out["lse"], causal, [(0, 0), (3, 17), (7, 31)])
-    check_bwd_units(q, k, v, do, out["dq"], out["dk"], out["dv"], causal, [(0, 5), (6, 30)], "fp16")
-    check_bwd_invariants(out["do"], out["dk"], out["dv"], 32, 32)
+    check_forward_units(q, k, v, out["o"], out["lse"], causal, all_units(8, 32))
+    check_backward_units(q, k, v, do, out["dq"], out["dk"], out["dv"], causal, spread(8, 32, 16))
+    check_bwd_invariants(do, out["dk"], out["dv"], 32, 32)
 
 
 def test_gqa_b4_h32_hkv8_l4096_d128_bf16_causal(cuda_lib):
     """Forward GQA causal, groups of 4 query heads per K/V head, bf16."""
     q, k, v, _ = make_qkv(4, 4096, 32, 8, 128, "bf16", seed=1, with_do=False)
     out = run_fwd_bwd(q, k, v, None, True, with_bwd=False)
-    check_fwd_units(q, k, v, out["o"], out["lse"], True, [(0, 0), (1, 3), (2, 4), (3, 31)])
+    check_forward_units(q, k, v, out["o"], out["lse"], True, spread(4, 32, 16))
 
 
 @pytest.mark.parametrize("causal", [False, True])
 def test_bwd_b8_h32_l1024_d64_fp16(cuda_lib, causal):
-    """Backward MHA B=8, H=32, L=1024, D=64 fp16, O and LSE from the forward."""
+    """Backward MHA B=8, H=32, L=1024, D=64 fp16, O and LSE from the forward: every unit."""
     q, k, v, do = make_qkv(8, 1024, 32, 32, 64, "fp16", seed=2 + int(causal))
     out = run_fwd_bwd(q, k, v, do, causal)
-    check_fwd_units(q, k, v, out["o"], out["lse"], causal, [(0, 0), (7, 31)])
-    check_bwd_units(q, k, v, do, out["dq"], out["dk"], out["dv"], causal,
-                    [(0, 0), (2, 9), (5, 20), (7, 31)], "fp16")
-    check_bwd_invariants(out["do"], out["dk"], out["dv"], 32, 32)
+    check_forward_units(q, k, v, out["o"], out["lse"], causal, all_units(8, 32))
+    check_backward_units(q, k, v, do, out["dq"], out["dk"], out["dv"], causal, all_units(8, 32))
+    check_bwd_invariants(do, out["dk"], out["dv"], 32, 32)
 
 
 @pytest.mark.parametrize("L", [1024, 4096, 8192, 16384])
 def test_long_sequence_b1_h32_d128_causal(cuda_lib, L):
-    """Long-sequence forward + backward, causal, B=1, H=32, D=128 (hidden 4096)."""
+    """Long-sequence forward + backward, causal, B=1, H=32, D=128 (hidden 4096):
+    every head up to L = 4096, sixteen forward and eight backward heads beyond."""
     q, k, v, do = make_qkv(1, L, 32, 32, 128, "fp16", seed=10 + L)
     out = run_fwd_bwd(q, k, v, do, True)
-    units = [(0, 0), (0, 31)] if L > 4096 else [(0, 0), (0, 13), (0, 31)]
-    check_fwd_units(q, k, v, out["o"], out["lse"], True, units)
-    check_bwd_units(q, k, v, do, out["dq"], out["dk"], out["dv"], True, units[:2], "fp16")
-    check_bwd_invariants(out["do"], out["dk"], out["dv"], 32, 32)
+    fwd_units = all_units(1, 32) if L <= 4096 else spread(1, 32, 16)
+    bwd_units = all_units(1, 32) if L <= 4096 else spread(1, 32, 8)
+    panel = 1024 if L > 8192 else 2048
+    check_forward_units(q, k, v, out["o"], out["lse"], True, fwd_units, panel=panel)
+    check_backward_units(q, k, v, do, out["dq"], out["dk"], out["dv"], True, bwd_units,
+                         panel=panel)
+    check_bwd_invariants(do, out["dk"], out["dv"], 32, 32)

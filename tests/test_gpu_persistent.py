@@ -12,7 +12,7 @@ import pytest
 import torch
 
 import tiled_attention_fa_gb300 as fa
-from tests.helpers import LSE_ATOL, assert_close, inputs, kernel_casts, to64
+from tests.helpers import LSE_ATOL, assert_close, check_backward, inputs, to64
 from tests.test_gpu_bwd import gpu_fwd_bwd
 from oracle import fa_oracle as orc
 
@@ -35,10 +35,7 @@ def test_backward_many_units_per_cta(cuda_lib, B, L, H, Hkv, D, dtype, causal):
     assert units(B, L, Hkv, causal) > sms, "shape must give some CTA more than one unit"
     (q, k, v, do), (qd, kd, vd, dod) = inputs(B, L, H, Hkv, D, dtype, seed=B * L + H + int(causal))
     _, _, dq, dk, dv, _ = gpu_fwd_bwd(qd, kd, vd, dod, causal)
-    rq, rk, rv, _ = orc.backward(q, k, v, do, causal, **kernel_casts(dtype))
-    assert_close(to64(dv), rv, name="dV")
-    assert_close(to64(dk), rk, name="dK")
-    assert_close(to64(dq), rq, name="dQ")
+    check_backward((to64(dq), to64(dk), to64(dv)), q, k, v, do, causal, dtype)
 
 
 def fwd_items(B, L, H):

@@ -525,49 +525,6 @@ def test_forward_cast_exact_when_weights_are_representable():
 
 
 @pytest.mark.parametrize("fmt,tdt", [("bf16", torch.bfloat16), ("fp16", torch.float16)])
-def test_cast_ds_only_moves_dq_dk(fmt, tdt):
-    # dS cast for the dK and dQ products: dQ = cast(dS) K / sqrt(D), dK = sum over the
-    # group of cast(dS)^T Q / sqrt(D), dS from torch's softmax; dV and Delta unchanged.
-    B, L, H, Hkv, D = 1, 35, 4, 2, 12   # 1/sqrt(12) is no power of two: the cast precedes it
-    q, k, v, do = (rnd((B, L, h, D), s) for h, s in ((H, 105), (Hkv, 106), (Hkv, 107), (H, 108)))
-    dq0, dk0, dv0, d0 = orc.backward(q, k, v, do, True)
-    dq1, dk1, dv1, d1 = orc.backward(q, k, v, do, True, ds_round=fmt)
-    np.testing.assert_array_equal(dv0, dv1)
-    np.testing.assert_array_equal(d0, d1)
-    qt, kt, vt, dot = (torch.from_numpy(x) for x in (q, k, v, do))
-    want_dk = torch.zeros(B, L, Hkv, D, dtype=torch.float64)
-    for h in range(H):
-        hk = h // (H // Hkv)
-        _, _, p, dp, o = _torch_unit(qt, kt, vt, dot, h, hk, True)
-        delta = (o * dot[0, :, h]).sum(dim=1, keepdim=True)
-        ds = (p * (dp - delta)).to(torch.float32).to(tdt).double()
-        np.testing.assert_allclose(dq1[0, :, h], (ds @ kt[0, :, hk] / math.sqrt(D)).numpy(),
-                                   rtol=1e-12, atol=1e-12)
-        want_dk[0, :, hk] += ds.T @ qt[0, :, h] / math.sqrt(D)
-    np.testing.assert_allclose(dk1, want_dk.numpy(), rtol=1e-12, atol=1e-12)
-    assert np.abs(dk1 - dk0).max() > 0 and np.abs(dq1 - dq0).max() > 0
-
-
-@pytest.mark.parametrize("zero", ["q", "k"])
-def test_cast_ds_exact_when_ds_is_representable(zero):
-    # Zero queries or zero keys, L = 8 keys (P = 1/8), V and dO in {0, 1}, D = 4: dP is
-    # an integer, Delta a multiple of 1/8 below 4, so dS = (dP - Delta)/8 has at most 6
-    # significant bits -- exact in bf16 and fp16.  Zero queries leave dQ = dS K nonzero,
-    # zero keys dK = dS^T Q.
-    B, L, H, D = 1, 8, 2, 4
-    rng = np.random.default_rng(109)
-    q, k = (rng.standard_normal((B, L, H, D)) for _ in range(2))
-    (q if zero == "q" else k)[:] = 0.0
-    v, do = (rng.integers(0, 2, (B, L, H, D)).astype(np.float64) for _ in range(2))
-    ref = orc.backward(q, k, v, do, False)
-    assert np.abs(ref[0 if zero == "q" else 1]).max() > 0
-    for fmt in ("bf16", "fp16"):
-        got = orc.backward(q, k, v, do, False, ds_round=fmt)
-        for a, b in zip(ref, got):
-            np.testing.assert_allclose(b, a, rtol=0, atol=1e-14)
-
-
-@pytest.mark.parametrize("fmt,tdt", [("bf16", torch.bfloat16), ("fp16", torch.float16)])
 def test_forward_cast_in_backward_moves_delta(fmt, tdt):
     # fwd_p_round forms the O behind Delta with the forward's cast: Delta is the row dot
     # product of (cast(exp(S - m)) V / l, stored) with dO; dV does not depend on Delta.
@@ -780,3 +737,71 @@ def test_fp8_inputs_are_seeded_codes_with_amax_scales():
     for codes, s in zip(a[:3], a[3:]):
         vals = orc.e4m3_decode(codes.numpy())
         assert not np.isnan(vals).any() and np.abs(vals).max() == 448.0 and s > 0
+
+
+# ---------------------------------------------------------------- intermediates for error bounds
+
+def _torch_scores_grad(q, k, v, do, causal):
+    """Independent torch float64 autograd of f = sum(O o dO) through the score matrix:
+    returns (P, dS = df/dS) for one unit, with S = Q K^T / sqrt(D), bottom-right causal."""
+    qt, kt, vt, dot = (torch.from_numpy(x) for x in (q, k, v, do))
+    Lq, Lk, D = q.shape[0], k.shape[0], q.shape[1]
+    s = (qt @ kt.T / math.sqrt(D)).detach().requires_grad_(True)
+    if causal:
+        mask = torch.arange(Lk)[None, :] > torch.arange(Lq)[:, None] + (Lk - Lq)
+        sm = s.masked_fill(mask, float("-inf"))
+    else:
+        sm = s
+    p = torch.softmax(sm, dim=1)
+    (p @ vt * dot).sum().backward()
+    return p.detach().numpy(), s.grad.numpy()
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("Lq,Lk", [(9, 9), (5, 13), (1, 4)])
+def test_unit_probs_match_torch_softmax(causal, Lq, Lk):
+    rng = np.random.default_rng(120 + Lq + Lk)
+    q, k = rng.standard_normal((Lq, 8)), rng.standard_normal((Lk, 8))
+    P, E, l = orc.unit_probs(q, k, causal)
+    want, _ = _torch_scores_grad(q, k, rng.standard_normal((Lk, 8)), rng.standard_normal((Lq, 8)),
+                                 causal)
+    np.testing.assert_allclose(P, want, rtol=1e-13, atol=1e-15)
+    np.testing.assert_allclose(E.max(axis=1), 1.0, rtol=0, atol=0)  # largest entry is exp(0)
+    np.testing.assert_allclose(E / l[:, None], P, rtol=1e-15, atol=0)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("Lq,Lk", [(11, 11), (6, 14)])
+def test_backward_parts_match_autograd(causal, Lq, Lk):
+    # dS is the gradient of sum(O o dO) with respect to the scores (torch autograd,
+    # independent of the oracle); its rows sum to zero; dQ, dK from the parts equal the
+    # finite-difference-pinned unit_backward.
+    rng = np.random.default_rng(130 + Lq + Lk + int(causal))
+    D = 8
+    q, k, v = rng.standard_normal((Lq, D)), rng.standard_normal((Lk, D)), rng.standard_normal((Lk, D))
+    do = rng.standard_normal((Lq, D))
+    parts = orc.unit_backward_parts(q, k, v, do, causal)
+    P, dS_ref = _torch_scores_grad(q, k, v, do, causal)
+    np.testing.assert_allclose(parts["P"], P, rtol=1e-13, atol=1e-15)
+    np.testing.assert_allclose(parts["dS"], dS_ref, rtol=1e-11, atol=1e-13)
+    np.testing.assert_allclose(parts["dS"].sum(axis=1), 0.0, atol=1e-13)
+    np.testing.assert_allclose(parts["dP"], do @ v.T, rtol=1e-14, atol=1e-14)
+    dq, dk, dv, delta, o, _ = orc.unit_backward(q, k, v, do, causal)
+    np.testing.assert_allclose(parts["O"], o, rtol=1e-13, atol=1e-14)
+    np.testing.assert_allclose(parts["Delta"], delta, rtol=1e-13, atol=1e-14)
+    np.testing.assert_allclose(parts["dS"] @ k / math.sqrt(D), dq, rtol=1e-12, atol=1e-13)
+    np.testing.assert_allclose(parts["dS"].T @ q / math.sqrt(D), dk, rtol=1e-12, atol=1e-13)
+    np.testing.assert_allclose(parts["P"].T @ do, dv, rtol=1e-12, atol=1e-13)
+
+
+def test_backward_parts_teeth():
+    # A dS without Delta, or with the probabilities transposed, breaks the zero row sums
+    # or the autograd comparison.
+    rng = np.random.default_rng(140)
+    q, k, v, do = (rng.standard_normal((10, 8)) for _ in range(4))
+    parts = orc.unit_backward_parts(q, k, v, do, True)
+    _, dS_ref = _torch_scores_grad(q, k, v, do, True)
+    no_delta = parts["P"] * parts["dP"]
+    assert np.abs(no_delta.sum(axis=1)).max() > 1e-3
+    transposed = parts["P"].T * (parts["dP"] - parts["Delta"][:, None])
+    assert np.abs(transposed - dS_ref).max() > 1e-3

@@ -43,10 +43,15 @@ def test_noalloc_matches_workspace_backward(cuda_lib, B, L, H, Hkv, D, causal):
     ref = [torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)]
     assert lib.fa_bwd(_p(q), _p(k), _p(v), _p(o), _p(do), _p(lse), _p(delta),
                       *(_p(t) for t in ref), _p(acc), 0, *dims, _stream()) == _lib.FA_OK
+    # The flow of a caller that allocates nothing: Delta from the preprocess
+    # with no accumulator, then the no-allocation backward.
+    delta2 = torch.full_like(lse, float("nan"))
+    assert lib.fa_bwd_preprocess(_p(o), _p(do), _p(delta2), None, B, L, H, D, _lib.FA_F16,
+                                 _stream()) == _lib.FA_OK
     for call in range(2):
         got = [torch.full_like(q, float("nan")), torch.full_like(k, float("nan")),
                torch.full_like(v, float("nan"))]
-        st = lib.fa_bwd_noalloc(_p(q), _p(k), _p(v), _p(o), _p(do), _p(lse), _p(delta),
+        st = lib.fa_bwd_noalloc(_p(q), _p(k), _p(v), _p(o), _p(do), _p(lse), _p(delta2),
                                 *(_p(t) for t in got), *dims, _stream())
         assert st == _lib.FA_OK, lib.fa_status_string(st)
         torch.cuda.synchronize()

@@ -156,17 +156,24 @@ float* g_noalloc_ptr[kMaxDevices] = {};
 
 // Device address of the scratch array on the current device.  In host code
 // the array's name is only a host-side stand-in, so the address is looked up
-// once per device (with that device current) and cached.
-fa_status noalloc_scratch(float** out) {
+// with the device current.  It is looked up again on every call whose stream
+// is not being captured (a device reset reloads the module, possibly at
+// another address) and remembered per device for calls made during a
+// capture, where the lookup is not attempted.
+fa_status noalloc_scratch(cudaStream_t s, float** out) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return FA_ERR_CUDA;
   if (dev < 0 || dev >= kMaxDevices) return FA_ERR_UNSUPPORTED;
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(s, &cs) != cudaSuccess) return FA_ERR_CUDA;
   std::lock_guard<std::mutex> lock(g_noalloc_mu);
-  if (g_noalloc_ptr[dev] == nullptr) {
+  if (cs == cudaStreamCaptureStatusNone) {
     void* ptr = nullptr;
     if (cudaGetSymbolAddress(&ptr, g_noalloc_dq_accum) != cudaSuccess || ptr == nullptr)
       return FA_ERR_CUDA;
     g_noalloc_ptr[dev] = static_cast<float*>(ptr);
+  } else if (g_noalloc_ptr[dev] == nullptr) {
+    return FA_ERR_CUDA;  // first call on this device made during a capture
   }
   *out = g_noalloc_ptr[dev];
   return FA_OK;
@@ -180,7 +187,7 @@ fa_status run_bwd_noalloc(const void* Q, const void* K, const void* V, const voi
   const size_t need = static_cast<size_t>(B) * H * padded_len(L) * D * sizeof(float);
   if (need > FA_NOALLOC_SCRATCH_BYTES) return FA_ERR_SCRATCH_TOO_SMALL;
   float* acc = nullptr;
-  fa_status st = noalloc_scratch(&acc);
+  fa_status st = noalloc_scratch(s, &acc);
   if (st != FA_OK) return st;
   // The array keeps the previous call's sums: clear the part this call uses.
   if (cudaMemsetAsync(acc, 0, need, s) != cudaSuccess) return FA_ERR_CUDA;
