@@ -35,6 +35,7 @@ def run_and_compare(B, L, H, Hkv, D, dtype, causal, seed):
     # tolerance (atol + rtol |O|) per element, so Delta is within
     # sum_d |dO_d| (atol + rtol |O_d|) of the exact value.
     ro, _ = orc.forward(q, k, v, causal)
+    rdelta = orc.bwd_preprocess(ro, do)
     bound = np.einsum("blhd->bhl", np.abs(do) * (1e-2 + 1e-2 * np.abs(ro)))
     assert np.all(np.abs(to64(delta) - rdelta) <= bound), "Delta"
 
