@@ -78,12 +78,12 @@ static fa_status launch_bwd(const void* Q, const void* K, const void* V, const v
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Ly::SMEM_ALLOC) !=
       cudaSuccess)
     return FA_ERR_CUDA;
-  if constexpr (D == 128) {
-    // The kernel moves 48 registers per thread from the producer / MMA
-    // warpgroup to the dQ drain warpgroup (setmaxnreg 80 / 176); that balances
-    // only when every thread starts with 128.  Any other allocation would
-    // leave the increase waiting for registers that never come back, so
-    // refuse to launch instead.
+  {
+    // The kernel re-balances registers between its warpgroups (setmaxnreg:
+    // Ly::REGS_COMPUTE twice, REGS_DRAIN, REGS_OTHER per thread); the budgets
+    // add up only when every thread starts with NTHREADS_REGS.  Any other
+    // allocation would leave an increase waiting for registers that never
+    // come back, so refuse to launch instead.
     static int num_regs = -1;
     static std::once_flag once;
     std::call_once(once, [&] {

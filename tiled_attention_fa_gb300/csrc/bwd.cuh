@@ -15,21 +15,27 @@
 //   warps 0-7  compute warps: each query half of a tile (columns 0-63, then
 //              64-127) is split over all eight, warp w taking 32 columns
 //              of key rows 32*(w%4).. (its TMEM lanes); a thread owns one
-//              key row and forms P^T = exp2(S^T*c - LSE*log2e) as soon as
-//              S^T lands, then dS^T = P^T o (dP^T - Delta) once dP^T does;
-//              both go back to TMEM over the chunk's S^T columns (A operands
-//              of dV += P^T dO and dK += dS^T Q) and dS^T also to a swizzled
-//              smem tile (read MN-major as the A operand of dQ = dS K).  At
-//              the end warps 0-3 write dK and warps 4-7 dV.
+//              key row and forms P^T = exp2(S^T*c - LSE*log2e) for both
+//              halves as soon as S^T lands, then dS^T = P^T o (dP^T - Delta)
+//              for both once dP^T does; both go back to TMEM over the
+//              chunk's S^T columns (A operands of dV += P^T dO and
+//              dK += dS^T Q) and dS^T also to a swizzled smem tile (read
+//              MN-major as the A operand of dQ = dS K).  At the end warps
+//              0-3 write dK and warps 4-7 dV.
 //   warps 8-11 dQ drain: thread r owns query row r; takes the whole dQ row
 //              from TMEM, releases the columns, then adds it into the fp32
 //              accumulator with paced 16-byte vector reductions.
 //   warp  12   TMA producer: K_j, V_j once per K/V tile (two slots at D = 64,
-//              so the next tile's load overlaps the current one); then Q_i,
-//              dO_i (and LSE_i, Delta_i) through a two-slot ring.
+//              so the next tile's load overlaps the current one); then dO_i
+//              and Q_i (with LSE_i, Delta_i) through a two-slot ring whose dO
+//              and Q halves are released separately (after their last
+//              readers, dV and dK).
 //   warp  13   TMEM allocator and MMA issuer (the warp runs the schedule,
 //              one elected lane issues the MMAs and their commits).
 //   warps 14-15 idle (they only lower their register budget with 12-13).
+// The S^T and dP^T tiles alternate between two TMEM regions with the tile
+// counter, so the next tile's S^T is issued as soon as the compute warps have
+// consumed this tile's dP^T, ahead of this tile's last dK and its dQ.
 // An MMA with both operands in shared memory reads them at the shared-memory
 // rate (128 B per clock: an M=128 N=128 K=16 step, 8 KB, takes its 64 tensor
 // cycles in reads alone), so the schedule keeps every operand it can in TMEM:
@@ -60,6 +66,7 @@
 #ifndef FA_BWD_PACE_D64
 #define FA_BWD_PACE_D64 1
 #endif
+
 
 namespace fa {
 
@@ -97,7 +104,8 @@ struct BwdLayout {
                        B_DPFULL = B_SFULL + 1, B_PFULL = B_DPFULL + 1, B_DSFULL = B_PFULL + 2,
                        B_DQFULL = B_DSFULL + 2, B_DQEMPTY = B_DQFULL + 1,
                        B_DKVFULL = B_DQEMPTY + 1, B_DONE = B_DKVFULL + 1, B_KVEMPTY = B_DONE + 1,
-                       NBAR = B_KVEMPTY + KVS;
+                       B_DOFULL = B_KVEMPTY + KVS, B_DOEMPTY = B_DOFULL + STAGES,
+                       NBAR = B_DOEMPTY + STAGES;
   static constexpr uint32_t BAR_OFF = 0;
   static constexpr uint32_t MISC_OFF = BAR_OFF + NBAR * 8;              // tmem slot, abort flag
   static constexpr uint32_t STAT_OFF = (MISC_OFF + 16 + 15) / 16 * 16;  // [STAGES][2][128] f32
@@ -110,13 +118,16 @@ struct BwdLayout {
   static constexpr uint32_t DO_OFF = Q_OFF + STAGES * TILE;   // [STAGES] tiles
   static constexpr uint32_t DS_OFF = DO_OFF + STAGES * TILE;  // 2 chunks (128 keys x 128 queries)
   static constexpr uint32_t SMEM_ALLOC = DS_OFF + 2 * CHUNK;
-  // TMEM columns: dK | dV | S^T (128 queries) | dP^T (128 queries).  The
-  // compute warps overwrite each 32-query chunk of S^T with P^T (16 columns of
-  // 16-bit pairs) and dS^T (the next 16), the A operands of the dV and dK
-  // products.  The dQ tile (N = D) goes into the dP^T columns once both query
-  // halves are consumed; the next tile's S^T never waits for the dQ drain,
-  // only its dP^T does.
-  static constexpr uint32_t TM_DK = 0, TM_DV = D, TM_S = 2 * D, TM_DP = 2 * D + 128;
+  // TMEM columns: dK | dV | R0 | R1, two 128-column regions that alternate
+  // with the CTA's tile counter g: S^T(g) goes into R[g % 2] and dP^T(g) into
+  // the other.  The compute warps overwrite each 32-query chunk of S^T with
+  // P^T (16 columns of 16-bit pairs) and dS^T (the next 16), the A operands
+  // of the dV and dK products; dQ(g) (N = D) then goes into R[g % 2] as well,
+  // and dP^T(g+1) into R[g % 2] once the drain holds dQ(g) in registers.  So
+  // S^T(g+1) needs only dP^T(g) consumed, and is issued before dK and dQ of
+  // tile g.
+  static constexpr uint32_t TM_DK = 0, TM_DV = D, TM_R0 = 2 * D, TM_R1 = 2 * D + 128;
+  __host__ __device__ static constexpr uint32_t tm_region(uint32_t g) { return (g & 1u) ? TM_R1 : TM_R0; }
   // At D = 64 K_j and V_j also live in TMEM (32 columns of 16-bit pairs each),
   // copied there once per K/V tile, so S^T and dP^T read only Q / dO from
   // shared memory (at D = 128 the columns are all taken).
@@ -127,10 +138,16 @@ struct BwdLayout {
   // Registers per thread at launch (65,536 / NTHREADS); the D = 128 register
   // split between warpgroups assumes exactly this many.
   static constexpr int NTHREADS_REGS = 65536 / NTHREADS;
+  // Register budgets per thread (setmaxnreg) of the compute warpgroups (two),
+  // the dQ drain warpgroup and the producer / MMA warpgroup; multiples of 8
+  // that sum, over four 128-thread warpgroups, to the launch allocation.
+  static constexpr uint32_t REGS_COMPUTE = 136, REGS_DRAIN = 160, REGS_OTHER = 80;
+  static_assert(2 * REGS_COMPUTE + REGS_DRAIN + REGS_OTHER == 4 * NTHREADS_REGS,
+                "register budgets must sum to the launch allocation");
   // The column plan and the shared-memory plan fit the hardware.
-  static_assert(TM_S >= TM_DV + D && TM_DP >= TM_S + 128 && TM_DP + 128 <= TMEM_COLS,
+  static_assert(TM_R0 >= TM_DV + D && TM_R1 >= TM_R0 + 128 && TM_R1 + 128 <= TMEM_COLS,
                 "TMEM regions overlap or overflow");
-  static_assert(!KV_TMEM || (TM_K >= TM_DP + 128 && TM_V + D / 2 <= TMEM_COLS),
+  static_assert(!KV_TMEM || (TM_K >= TM_R1 + 128 && TM_V + D / 2 <= TMEM_COLS),
                 "TMEM copies of K / V overlap or overflow");
   static_assert(SMEM_ALLOC <= 232448, "shared memory beyond the 227 KB per-block limit");
 };
@@ -180,7 +197,10 @@ __device__ __forceinline__ void bwd_tile(const BwdItem& it, const BwdParams& p, 
                                          int& i) {
   const int per = p.n_q - it.i0;
   const int g = n / per;
-  i = it.i0 + (n - g * per);
+  // The CTA of K/V tile j starts at the j-th of its Q tiles and wraps around,
+  // so the CTAs working on one head at the same time read different Q / dO
+  // tiles and add into different dQ accumulator tiles.
+  i = it.i0 + (n - g * per + it.j) % per;
   h = it.hkv * (p.H / p.Hkv) + g;
 }
 
@@ -217,6 +237,8 @@ __global__ void __launch_bounds__(512, 1)
     for (int s = 0; s < Ly::STAGES; ++s) {
       mbar_init(bar(Ly::B_QFULL + s), 1);
       mbar_init(bar(Ly::B_QEMPTY + s), 1);
+      mbar_init(bar(Ly::B_DOFULL + s), 1);
+      mbar_init(bar(Ly::B_DOEMPTY + s), 1);
     }
     mbar_init(bar(Ly::B_SFULL), 1);
     mbar_init(bar(Ly::B_DPFULL), 1);
@@ -252,18 +274,19 @@ __global__ void __launch_bounds__(512, 1)
   // K_j / V_j of the next item load once the last MMA reading the current ones
   // completes (K/V-empty barrier).
   const int G = static_cast<int>(gridDim.x);
-  // At D = 128 the drain warpgroup (warps 8-11) holds a whole 128-column dQ
-  // row in registers; the producer / MMA warpgroup (12-15) needs few.  Budgets
-  // 128 + 128 + 176 + 80 registers per thread of each warpgroup's 128 threads
-  // sum to the launch total of 512 x 128.  Each role sets its budget first
-  // thing in its own branch, so the compiler allocates that branch to it.
-  constexpr bool kSplitRegs = (D == 128);
+  // Registers per thread are re-balanced between the warpgroups: the compute
+  // warpgroups (warps 0-7) hold both query halves' fp32 P^T between the
+  // exponent and dS phases, the drain warpgroup (warps 8-11) a whole dQ row,
+  // the producer / MMA warpgroup (12-15) needs few.  The four budgets sum to
+  // the launch total of 512 x 128 (Ly::REGS_*).  Each role sets its budget
+  // first thing in its own branch, so the compiler allocates that branch to it.
+  constexpr bool kSplitRegs = true;
 
   if (warp == 12) {
-    if constexpr (kSplitRegs) setmaxnreg_dec<80>();
+    if constexpr (kSplitRegs) setmaxnreg_dec<Ly::REGS_OTHER>();
     // ------------------------------------------------------------ producer (whole warp)
     bool ok = true;
-    uint32_t issued[Ly::STAGES] = {0, 0};
+    uint32_t issued[Ly::STAGES] = {0, 0}, issued_do[Ly::STAGES] = {0, 0};
     uint32_t stage = 0, phase = 0, kv_cnt = 0;
     for (int u = p.ipu * static_cast<int>(blockIdx.x); ok && u < p.ipu * p.n_units;
          u += (u % p.ipu == p.ipu - 1) ? p.ipu * (G - 1) + 1 : 1) {
@@ -290,6 +313,16 @@ __global__ void __launch_bounds__(512, 1)
     for (int n = 0; n < it.ntiles; ++n) {
       int h, i;
       bwd_tile(it, p, n, h, i);
+      // dO_i first: its slot frees after the previous occupant's last dV,
+      // before Q's (its last dK).
+      if (!mbar_wait_warp(bar(Ly::B_DOEMPTY + stage), phase ^ 1u, ab, err, 403)) { ok = false; break; }
+      if (lane == 0) {
+        mbar_arrive_expect_tx(bar(Ly::B_DOFULL + stage), Ly::TILE);
+        for (int c = 0; c < Ly::KCH; ++c)
+          tma_load_4d(base + Ly::DO_OFF + stage * Ly::TILE + c * Ly::CHUNK, &tmdO,
+                      bar(Ly::B_DOFULL + stage), c * 64, h, i * 128, it.b);
+      }
+      ++issued_do[stage];
       if (!mbar_wait_warp(bar(Ly::B_QEMPTY + stage), phase ^ 1u, ab, err, 401)) { ok = false; break; }
       // -LSE (pre-multiplied by log2 e) and -Delta of the 128 query rows of tile i.
       float* st = stats + stage * 256;
@@ -304,13 +337,10 @@ __global__ void __launch_bounds__(512, 1)
       }
       __syncwarp();  // every lane's LSE / Delta entries precede the arrival
       if (lane == 0) {
-        mbar_arrive_expect_tx(bar(Ly::B_QFULL + stage), 2 * Ly::TILE);
-        for (int c = 0; c < Ly::KCH; ++c) {
+        mbar_arrive_expect_tx(bar(Ly::B_QFULL + stage), Ly::TILE);
+        for (int c = 0; c < Ly::KCH; ++c)
           tma_load_4d(base + Ly::Q_OFF + stage * Ly::TILE + c * Ly::CHUNK, &tmQ,
                       bar(Ly::B_QFULL + stage), c * 64, h, i * 128, it.b);
-          tma_load_4d(base + Ly::DO_OFF + stage * Ly::TILE + c * Ly::CHUNK, &tmdO,
-                      bar(Ly::B_QFULL + stage), c * 64, h, i * 128, it.b);
-        }
       }
       ++issued[stage];
       if (++stage == Ly::STAGES) {
@@ -322,14 +352,23 @@ __global__ void __launch_bounds__(512, 1)
     if (!ok && lane == 0) {
       for (uint32_t c = kv_cnt > Ly::KVS ? kv_cnt - Ly::KVS : 0; c < kv_cnt; ++c)
         mbar_wait_drain(bar(Ly::B_KVFULL + c % Ly::KVS), (c / Ly::KVS) & 1);
-      for (int s = 0; s < Ly::STAGES; ++s)
+      for (int s = 0; s < Ly::STAGES; ++s) {
         if (issued[s] > 0) mbar_wait_drain(bar(Ly::B_QFULL + s), (issued[s] - 1) & 1);
+        if (issued_do[s] > 0) mbar_wait_drain(bar(Ly::B_DOFULL + s), (issued_do[s] - 1) & 1);
+      }
     }
   } else if (warp == 13) {
-    if constexpr (kSplitRegs) setmaxnreg_dec<80>();
+    if constexpr (kSplitRegs) setmaxnreg_dec<Ly::REGS_OTHER>();
     // ------------------------------------------------------------ MMA issuer
     // The whole warp runs the schedule (warp-uniform loop state and operand
     // descriptors); one elected lane issues each MMA group and the commits.
+    // Per tile g (regions: Ra = R[g % 2], Rb = the other):
+    //   [S^T(g) -> Ra, issued at the end of tile g-1, or here for an item's
+    //   first tile]  dP^T(g) -> Rb (after the drain holds dQ(g-1))
+    //   dV_A, dV_B (as each query half's P^T lands)  dK_A (its dS^T)
+    //   [once dS^T_B is in: S^T(g+1) -> Rb, whose dP^T(g) is consumed]
+    //   dK_B  dQ(g) = dS K -> Ra
+    // so the compute warps start on tile g+1 while dK_B(g) and dQ(g) run.
     auto commit = [&](int b) {
       if (elect_one()) tc_commit(bar(b));
       __syncwarp();
@@ -341,6 +380,22 @@ __global__ void __launch_bounds__(512, 1)
     uint64_t kd = 0, vd = 0, kd_mn = 0;  // the current K/V slot's (set per item)
     const uint64_t dsd_mn = sdesc_sw128(base + Ly::DS_OFF, Ly::CHUNK, 1024);
     auto koff = [](int k) -> uint64_t { return ((k >> 2) * Ly::CHUNK + (k & 3) * 32u) >> 4; };
+    // S^T(gg) = K_j Q^T of the Q tile in ring stage st into R[gg % 2].  The
+    // region's previous contents (dP^T(gg-1), dQ(gg-2)) were consumed before.
+    auto issue_s = [&](uint32_t st, uint32_t gg) {
+      const uint64_t qd = sdesc_sw128(base + Ly::Q_OFF + st * Ly::TILE, 16, 1024);
+      const uint32_t dst = tmem + Ly::tm_region(gg);
+      if (elect_one()) {
+#pragma unroll
+        for (int k = 0; k < D / 16; ++k)
+          if constexpr (Ly::KV_TMEM)
+            mma_ts(dst, tmem + Ly::TM_K + 8 * k, qd + koff(k), IDESC_S, k > 0 ? 1u : 0u);
+          else
+            mma_ss(dst, kd + koff(k), qd + koff(k), IDESC_S, k > 0 ? 1u : 0u);
+        tc_commit(bar(Ly::B_SFULL));
+      }
+      __syncwarp();
+    };
     for (int u = p.ipu * static_cast<int>(blockIdx.x); ok && u < p.ipu * p.n_units;
          u += (u % p.ipu == p.ipu - 1) ? p.ipu * (G - 1) + 1 : 1) {
     int item;
@@ -367,44 +422,34 @@ __global__ void __launch_bounds__(512, 1)
       }
       __syncwarp();
     }
-    // n: tile within the item (accumulate flags); g: tile of the CTA (phases)
+    // n: tile within the item (accumulate flags); g: tile of the CTA (phases, regions)
     for (int n = 0; ok && n < it.ntiles; ++n, ++g) {
-      if (!mbar_wait_warp(bar(Ly::B_QFULL + stage), phase, ab, err, 502)) { ok = false; break; }
-      tc_fence_after();
+      const uint32_t ra = tmem + Ly::tm_region(g), rb = tmem + Ly::tm_region(g + 1);
+      if (n == 0) {  // an item's first S^T (later ones are issued a tile ahead)
+        if (!mbar_wait_warp(bar(Ly::B_QFULL + stage), phase, ab, err, 502)) { ok = false; break; }
+        tc_fence_after();
+        issue_s(stage, g);
+      }
       const uint32_t qa = base + Ly::Q_OFF + stage * Ly::TILE;
       const uint32_t doa = base + Ly::DO_OFF + stage * Ly::TILE;
-      const uint64_t qd = sdesc_sw128(qa, 16, 1024), qd_mn = sdesc_sw128(qa, Ly::CHUNK, 1024);
+      const uint64_t qd_mn = sdesc_sw128(qa, Ly::CHUNK, 1024);
       const uint64_t dod = sdesc_sw128(doa, 16, 1024), dod_mn = sdesc_sw128(doa, Ly::CHUNK, 1024);
-      // S^T = K_j Q_i^T: the previous tile's P^T / dS^T in these columns are
-      // read by MMAs issued before, which run first.
+      // dP^T = V_j dO_i^T into Rb, once the drain holds the previous dQ tile
+      // (which occupied these columns) in registers.
+      if (!mbar_wait_warp(bar(Ly::B_DOFULL + stage), phase, ab, err, 512)) { ok = false; break; }
+      if (g > 0 && !mbar_wait_warp(bar(Ly::B_DQEMPTY), (g - 1) & 1, ab, err, 503)) { ok = false; break; }
+      tc_fence_after();
       if (elect_one()) {
 #pragma unroll
         for (int k = 0; k < D / 16; ++k)
           if constexpr (Ly::KV_TMEM)
-            mma_ts(tmem + Ly::TM_S, tmem + Ly::TM_K + 8 * k, qd + koff(k), IDESC_S, k > 0 ? 1u : 0u);
+            mma_ts(rb, tmem + Ly::TM_V + 8 * k, dod + koff(k), IDESC_S, k > 0 ? 1u : 0u);
           else
-            mma_ss(tmem + Ly::TM_S, kd + koff(k), qd + koff(k), IDESC_S, k > 0 ? 1u : 0u);
-        tc_commit(bar(Ly::B_SFULL));
-      }
-      __syncwarp();
-      // dP^T = V_j dO_i^T, once the drain holds the previous dQ tile (which
-      // occupied these columns) in registers.
-      if (g > 0) {
-        if (!mbar_wait_warp(bar(Ly::B_DQEMPTY), (g - 1) & 1, ab, err, 503)) { ok = false; break; }
-        tc_fence_after();
-      }
-      if (elect_one()) {
-#pragma unroll
-        for (int k = 0; k < D / 16; ++k)
-          if constexpr (Ly::KV_TMEM)
-            mma_ts(tmem + Ly::TM_DP, tmem + Ly::TM_V + 8 * k, dod + koff(k), IDESC_S, k > 0 ? 1u : 0u);
-          else
-            mma_ss(tmem + Ly::TM_DP, vd + koff(k), dod + koff(k), IDESC_S, k > 0 ? 1u : 0u);
+            mma_ss(rb, vd + koff(k), dod + koff(k), IDESC_S, k > 0 ? 1u : 0u);
         tc_commit(bar(Ly::B_DPFULL));
       }
       __syncwarp();
-      // dV += P^T_c dO_c as each query half's P^T lands in TMEM, dK += dS^T_c
-      // Q_c as its dS^T does (both A operands from TMEM).
+      // dV += P^T_c dO_c as each query half's P^T lands in TMEM (A operand from TMEM).
 #pragma unroll
       for (int c = 0; c < 2; ++c) {
         if (!mbar_wait_warp(bar(Ly::B_PFULL + c), g & 1, ab, err, 504 + c)) { ok = false; break; }
@@ -412,32 +457,49 @@ __global__ void __launch_bounds__(512, 1)
         if (elect_one()) {
 #pragma unroll
           for (int k = 0; k < 4; ++k)
-            mma_ts(tmem + Ly::TM_DV, tmem + Ly::TM_S + 64 * c + (k >> 1) * 32u + (k & 1) * 8u,
+            mma_ts(tmem + Ly::TM_DV, ra + 64 * c + (k >> 1) * 32u + (k & 1) * 8u,
                    dod_mn + ((2048u * (4 * c + k)) >> 4), IDESC_KN,
                    (n > 0 || c > 0 || k > 0) ? 1u : 0u);
+          if (c == 1) tc_commit(bar(Ly::B_DOEMPTY + stage));  // dV_B was dO_i's last reader
         }
         __syncwarp();
+      }
+      if (!ok) break;
+      // dK += dS^T_c Q_c as each half's dS^T lands.  Once the second half is
+      // in, the compute warps have consumed dP^T(g): the next tile's S^T goes
+      // into Rb first, then dK_B and dQ(g) follow.
+      const bool more = n + 1 < it.ntiles;
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
         if (!mbar_wait_warp(bar(Ly::B_DSFULL + c), g & 1, ab, err, 508 + c)) { ok = false; break; }
         tc_fence_after();
+        if (c == 1 && more) {
+          const uint32_t ns = stage + 1 == Ly::STAGES ? 0 : stage + 1;
+          const uint32_t nph = stage + 1 == Ly::STAGES ? phase ^ 1u : phase;
+          if (!mbar_wait_warp(bar(Ly::B_QFULL + ns), nph, ab, err, 511)) { ok = false; break; }
+          tc_fence_after();
+          issue_s(ns, g + 1);
+        }
         if (elect_one()) {
 #pragma unroll
           for (int k = 0; k < 4; ++k)
-            mma_ts(tmem + Ly::TM_DK, tmem + Ly::TM_S + 64 * c + (k >> 1) * 32u + 16u + (k & 1) * 8u,
+            mma_ts(tmem + Ly::TM_DK, ra + 64 * c + (k >> 1) * 32u + 16u + (k & 1) * 8u,
                    qd_mn + ((2048u * (4 * c + k)) >> 4), IDESC_KN,
                    (n > 0 || c > 0 || k > 0) ? 1u : 0u);
         }
         __syncwarp();
       }
       if (!ok) break;
-      // dQ_i = dS K_j into the consumed dP^T columns (dS read MN-major from
-      // the dS^T tile in shared memory, K_j MN-major)
+      // Q_i is no longer read (dK_B was its last reader).
+      commit(Ly::B_QEMPTY + stage);
+      // dQ_i = dS K_j into Ra (dS read MN-major from the dS^T tile in shared
+      // memory, K_j MN-major); the P^T / dS^T there are read by the MMAs above.
       if (elect_one()) {
 #pragma unroll
         for (int k = 0; k < 8; ++k)
-          mma_ss(tmem + Ly::TM_DP, dsd_mn + ((2048u * k) >> 4), kd_mn + ((2048u * k) >> 4),
-                 IDESC_MN, k > 0 ? 1u : 0u);
+          mma_ss(ra, dsd_mn + ((2048u * k) >> 4), kd_mn + ((2048u * k) >> 4), IDESC_MN,
+                 k > 0 ? 1u : 0u);
         tc_commit(bar(Ly::B_DQFULL));
-        tc_commit(bar(Ly::B_QEMPTY + stage));
       }
       __syncwarp();
       if (++stage == Ly::STAGES) {
@@ -457,10 +519,13 @@ __global__ void __launch_bounds__(512, 1)
     commit(Ly::B_DONE);
     mbar_wait_drain(bar(Ly::B_DONE), 0);
   } else if (warp < 8) {
+    if constexpr (kSplitRegs) setmaxnreg_inc<Ly::REGS_COMPUTE>();
     // ------------------------------------------------------------ P^T / dS^T
-    // All eight warps work on query half A, then on half B: warp w owns key
-    // rows 32*(w%4).. (its TMEM lanes) and the 32-query chunk sub = w/4 of the
-    // current half.
+    // All eight warps work on each query half in turn: warp w owns key rows
+    // 32*(w%4).. (its TMEM lanes) and the 32-query chunk sub = w/4 of the
+    // half.  Per tile: P^T of half A, then of half B (from S^T alone, which
+    // lands first), then dS^T of half A and of half B (once dP^T lands); the
+    // fp32 P^T of both halves stays in registers in between.
     const int sub = warp >> 2;        // 32-query chunk within a half
     const int r = threadIdx.x & 127;  // key row within the tile == TMEM lane
     const uint32_t lane_off = ((warp & 3u) * 32u) << 16;
@@ -476,13 +541,16 @@ __global__ void __launch_bounds__(512, 1)
     for (int n = 0; ok && n < it.ntiles; ++n, ++g) {
       int h, i;
       bwd_tile(it, p, n, h, i);
+      // S^T(g) and then P^T / dS^T in region R[g % 2]; dP^T(g) in the other.
+      const uint32_t tSr = tmem + lane_off + Ly::tm_region(g);
+      const uint32_t tPr = tmem + lane_off + Ly::tm_region(g + 1);
       if (!mbar_wait_warp(bar(Ly::B_SFULL), g & 1, ab, err, 601)) { ok = false; break; }
       tc_fence_after();
+      uint32_t pf[2][32];  // P^T of each half in fp32, for dS^T
 #pragma unroll
       for (int hc = 0; hc < 2; ++hc) {
         const int cbase = 64 * hc + 32 * sub;  // first query column of this chunk
-        const uint32_t tS = tmem + lane_off + Ly::TM_S + cbase;
-        const uint32_t tP = tmem + lane_off + Ly::TM_DP + cbase;
+        const uint32_t tS = tSr + cbase;
         const float* st = stats + stage * 256 + cbase;
         const int q0 = i * 128 + cbase;
         // query columns [lo, hi) of this chunk are visible to key kr
@@ -490,9 +558,8 @@ __global__ void __launch_bounds__(512, 1)
         if (kr >= p.Lk) hi = 0;
         if (p.causal) lo = max(0, kr - p.past - q0);
         const bool full = (lo == 0 && hi == 32);
-        // Phase 1, from S^T alone (dP^T may still be in the tensor core):
-        // P^T = exp2(S^T*c - LSE*log2e).
-        uint32_t sv[32];
+        // P^T = exp2(S^T*c - LSE*log2e), from S^T alone.
+        uint32_t* sv = pf[hc];
         tmem_ld32(tS, sv);
         tmem_ld_wait32(sv);
         uint32_t pk[16];
@@ -514,7 +581,7 @@ __global__ void __launch_bounds__(512, 1)
                 p0 = (cl >= lo && cl < hi) ? p0 : 0.f;
                 p1 = (cl + 1 >= lo && cl + 1 < hi) ? p1 : 0.f;
               }
-              sv[cl] = __float_as_uint(p0);  // P^T in fp32 for phase 2
+              sv[cl] = __float_as_uint(p0);  // P^T in fp32 for dS^T
               sv[cl + 1] = __float_as_uint(p1);
               pk[cl >> 1] = pack2<T>(p0, p1);
             }
@@ -530,13 +597,18 @@ __global__ void __launch_bounds__(512, 1)
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(Ly::B_PFULL + hc));
-        // Phase 2: dS^T = P^T o (dP^T - Delta).
-        if (hc == 0) {
-          if (!mbar_wait_warp(bar(Ly::B_DPFULL), g & 1, ab, err, 602)) { ok = false; break; }
-          tc_fence_after();
-        }
+      }
+      if (!mbar_wait_warp(bar(Ly::B_DPFULL), g & 1, ab, err, 602)) { ok = false; break; }
+      tc_fence_after();
+#pragma unroll
+      for (int hc = 0; hc < 2; ++hc) {
+        // dS^T = P^T o (dP^T - Delta).
+        const int cbase = 64 * hc + 32 * sub;
+        const uint32_t tS = tSr + cbase;
+        const float* st = stats + stage * 256 + cbase;
+        const uint32_t* sv = pf[hc];
         uint32_t dp[32];
-        tmem_ld32(tP, dp);
+        tmem_ld32(tPr + cbase, dp);
         tmem_ld_wait32(dp);
         uint32_t dk[16];
         const uint4* nd4 = reinterpret_cast<const uint4*>(st + 128);  // -Delta
@@ -571,7 +643,6 @@ __global__ void __launch_bounds__(512, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(Ly::B_DSFULL + hc));
       }
-      if (!ok) break;
       if (++stage == Ly::STAGES) stage = 0;
     }
     const int hc = sub;  // epilogue role: warps 0-3 write dK, warps 4-7 write dV
@@ -605,7 +676,7 @@ __global__ void __launch_bounds__(512, 1)
     ++kv_cnt;
     }
   } else if (warp < 12) {
-    if constexpr (kSplitRegs) setmaxnreg_inc<176>();
+    if constexpr (kSplitRegs) setmaxnreg_inc<Ly::REGS_DRAIN>();
     // ------------------------------------------------------------ dQ drain
     const int r = threadIdx.x & 127;  // query row within the Q tile == TMEM lane
     const uint32_t lane_off = ((warp & 3u) * 32u) << 16;
@@ -629,8 +700,9 @@ __global__ void __launch_bounds__(512, 1)
       // The whole dQ row (D fp32) in registers, then its columns go back to
       // the MMA warp before any reduction is issued.
       uint32_t gq[D];
+      const uint32_t tq = tmem + lane_off + Ly::tm_region(g);  // dQ(g) lies in R[g % 2]
 #pragma unroll
-      for (int cc = 0; cc < D / 32; ++cc) tmem_ld32(tmem + lane_off + Ly::TM_DP + 32 * cc, gq + 32 * cc);
+      for (int cc = 0; cc < D / 32; ++cc) tmem_ld32(tq + 32 * cc, gq + 32 * cc);
 #pragma unroll
       for (int cc = 0; cc < D / 32; ++cc) tmem_ld_wait32(gq + 32 * cc);
       tc_fence_before();
@@ -641,13 +713,13 @@ __global__ void __launch_bounds__(512, 1)
         for (int c4 = 0; c4 < D / 4; ++c4) {
           // Paced: issued back to back, a tile's reductions hold the SM's
           // memory-instruction path for ~1,000 cycles and slow the MMAs that
-          // read shared memory meanwhile (the next tile's S^T and dP^T).  At
-          // B8 H32 L4096 D128 (a tile every ~2.5 us): a 128 ns pause after
-          // every second reduction (15 pauses, ~1.9 us) 4.15 ms; 64 ns after
-          // each 4.24; 32 ns after each 4.66; 64 ns after every second 4.96;
-          // unpaced 5.60 on an earlier build.  Bursts of more than four, or
-          // pauses adding up to the tile time, are slower.  __nanosleep(t)
-          // sleeps for the power of two above t.
+          // read shared memory meanwhile.  Measured at B8 H32 L4096 D128 fp16
+          // (a tile every ~2.5 us, 2070 MHz): no pause 5.3-5.6 ms; a pause
+          // after every second reduction (15 pauses) requested as 64 ns or
+          // 100 ns 4.46 ms, as 128 ns 7.31 ms (the pauses then outlast the
+          // tile and the drain holds up the next dP^T); 50 ns after each
+          // 4.52; 200 ns after every eighth 5.60.  (__nanosleep's duration
+          // is only approximately its argument.)
           if ((D == 128 || FA_BWD_PACE_D64) && FA_BWD_PACE_NS > 0 &&
               (c4 % FA_BWD_PACE_EVERY) == FA_BWD_PACE_EVERY - 1 && c4 < D / 4 - 1)
             __nanosleep(FA_BWD_PACE_NS);
@@ -660,7 +732,7 @@ __global__ void __launch_bounds__(512, 1)
     }
   } else {
     // warps 14-15: idle, but they belong to the producer / MMA warpgroup
-    if constexpr (kSplitRegs) setmaxnreg_dec<80>();
+    if constexpr (kSplitRegs) setmaxnreg_dec<Ly::REGS_OTHER>();
   }
 
   tc_fence_before();
@@ -729,39 +801,52 @@ __global__ void __launch_bounds__(256)
 }
 
 // ---------------------------------------------------------------- dQ post-process
-// One CTA per (batch, head, 64-row chunk): reads the accumulator chunk
-// (column groups of 64 contiguous float4), transposes through shared memory,
-// scales by 1/sqrt(D) and writes BSHD rows.
+// One CTA per (batch, head, 64-row chunk): every thread first loads its share
+// of the accumulator chunk (column groups of 64 contiguous float4, read once,
+// streaming), then the chunk is transposed through shared memory with 16-byte
+// accesses, scaled by 1/sqrt(D) and written as BSHD rows.
 template <int D, bool BF16>
 __global__ void __launch_bounds__(256)
     fa_dq_convert_kernel(const float* __restrict__ dq_accum, void* __restrict__ dQ, int B, int L,
                          int H, int Lpad, float scale) {
   using T = typename std::conditional<BF16, __nv_bfloat16, __half>::type;
-  __shared__ float tile[64][D + 4];
+  constexpr int RS = D + 4;                 // row stride in floats (16-byte aligned, skewed banks)
+  constexpr int PER = (D / 4) * 64 / 256;   // float4 loads per thread
+  __shared__ __align__(16) float tile[64 * RS];
   const int chunks = Lpad / 64;
   const int bh = blockIdx.x / chunks;
   const int l0 = (blockIdx.x - bh * chunks) * 64;
   const int b = bh / H, h = bh - b * H;
   const float4* src = reinterpret_cast<const float4*>(dq_accum) + static_cast<size_t>(bh) * (D / 4) * Lpad + l0;
-  for (int idx = threadIdx.x; idx < (D / 4) * 64; idx += 256) {
+  float4 v[PER];
+#pragma unroll
+  for (int k = 0; k < PER; ++k) {
+    const int idx = threadIdx.x + 256 * k;
     const int c4 = idx / 64, l = idx - c4 * 64;
-    const float4 v = src[static_cast<size_t>(c4) * Lpad + l];
-    tile[l][4 * c4 + 0] = v.x;
-    tile[l][4 * c4 + 1] = v.y;
-    tile[l][4 * c4 + 2] = v.z;
-    tile[l][4 * c4 + 3] = v.w;
+    v[k] = __ldcs(src + static_cast<size_t>(c4) * Lpad + l);
+  }
+#pragma unroll
+  for (int k = 0; k < PER; ++k) {
+    const int idx = threadIdx.x + 256 * k;
+    const int c4 = idx / 64, l = idx - c4 * 64;
+    *reinterpret_cast<float4*>(tile + l * RS + 4 * c4) = v[k];
   }
   __syncthreads();
-  constexpr int UPR = D / 8;  // 16-byte units per output row
-  for (int idx = threadIdx.x; idx < 64 * UPR; idx += 256) {
+  constexpr int UPR = D / 8;  // 16-byte output units per row
+#pragma unroll
+  for (int k = 0; k < 64 * UPR / 256; ++k) {
+    const int idx = threadIdx.x + 256 * k;
     const int l = idx / UPR, u = idx - l * UPR;
     if (l0 + l >= L) continue;
-    uint32_t pk[4];
-#pragma unroll
-    for (int e = 0; e < 4; ++e)
-      pk[e] = pack2<T>(tile[l][8 * u + 2 * e] * scale, tile[l][8 * u + 2 * e + 1] * scale);
+    const float4 a = *reinterpret_cast<const float4*>(tile + l * RS + 8 * u);
+    const float4 c = *reinterpret_cast<const float4*>(tile + l * RS + 8 * u + 4);
+    uint4 o;
+    o.x = pack2<T>(a.x * scale, a.y * scale);
+    o.y = pack2<T>(a.z * scale, a.w * scale);
+    o.z = pack2<T>(c.x * scale, c.y * scale);
+    o.w = pack2<T>(c.z * scale, c.w * scale);
     T* row = reinterpret_cast<T*>(dQ) + ((static_cast<size_t>(b) * L + l0 + l) * H + h) * D;
-    reinterpret_cast<uint4*>(row)[u] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+    __stcs(reinterpret_cast<uint4*>(row) + u, o);
   }
 }
 
