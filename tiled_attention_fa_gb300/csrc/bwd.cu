@@ -100,7 +100,13 @@ static fa_status launch_bwd(const void* Q, const void* K, const void* V, const v
 template <int D, bool BF16>
 static fa_status launch_post(const float* dq_accum, void* dQ, int B, int L, int H, cudaStream_t s) {
   const int Lpad = padded_len(L);
-  fa_dq_convert_kernel<D, BF16><<<B * H * (Lpad / 64), 256, 0, s>>>(
+  auto kern = fa_dq_convert_kernel<D, BF16>;
+  constexpr size_t smem = conv_smem_bytes<D>();
+  if (smem > 48 * 1024 &&
+      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+          cudaSuccess)
+    return FA_ERR_CUDA;
+  kern<<<B * H * (Lpad / kConvRows), kConvThreads, smem, s>>>(
       dq_accum, dQ, B, L, H, Lpad, 1.f / sqrtf(static_cast<float>(D)));
   return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }

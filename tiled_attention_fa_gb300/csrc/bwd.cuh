@@ -68,6 +68,7 @@
 #endif
 
 
+
 namespace fa {
 
 struct BwdParams {
@@ -801,41 +802,47 @@ __global__ void __launch_bounds__(256)
 }
 
 // ---------------------------------------------------------------- dQ post-process
-// One CTA per (batch, head, 64-row chunk): every thread first loads its share
-// of the accumulator chunk (column groups of 64 contiguous float4, read once,
-// streaming), then the chunk is transposed through shared memory with 16-byte
-// accesses, scaled by 1/sqrt(D) and written as BSHD rows.
+// One CTA per (batch, head, chunk of CR rows): every thread first loads its
+// share of the accumulator chunk (column groups of CR contiguous float4, read
+// once, streaming), then the chunk is transposed through shared memory with
+// 16-byte accesses, scaled by 1/sqrt(D) and written as BSHD rows.
+constexpr int kConvRows = 64;                 // accumulator rows per CTA
+constexpr int kConvThreads = 4 * kConvRows;
+template <int D>
+constexpr size_t conv_smem_bytes() { return static_cast<size_t>(kConvRows) * (D + 4) * sizeof(float); }
+
 template <int D, bool BF16>
-__global__ void __launch_bounds__(256)
+__global__ void __launch_bounds__(kConvThreads)
     fa_dq_convert_kernel(const float* __restrict__ dq_accum, void* __restrict__ dQ, int B, int L,
                          int H, int Lpad, float scale) {
   using T = typename std::conditional<BF16, __nv_bfloat16, __half>::type;
+  constexpr int CR = kConvRows, NT = kConvThreads;
   constexpr int RS = D + 4;                 // row stride in floats (16-byte aligned, skewed banks)
-  constexpr int PER = (D / 4) * 64 / 256;   // float4 loads per thread
-  __shared__ __align__(16) float tile[64 * RS];
-  const int chunks = Lpad / 64;
+  constexpr int PER = (D / 4) * CR / NT;    // float4 loads per thread
+  extern __shared__ __align__(16) float tile[];  // [CR][RS]
+  const int chunks = Lpad / CR;
   const int bh = blockIdx.x / chunks;
-  const int l0 = (blockIdx.x - bh * chunks) * 64;
+  const int l0 = (blockIdx.x - bh * chunks) * CR;
   const int b = bh / H, h = bh - b * H;
   const float4* src = reinterpret_cast<const float4*>(dq_accum) + static_cast<size_t>(bh) * (D / 4) * Lpad + l0;
   float4 v[PER];
 #pragma unroll
   for (int k = 0; k < PER; ++k) {
-    const int idx = threadIdx.x + 256 * k;
-    const int c4 = idx / 64, l = idx - c4 * 64;
+    const int idx = threadIdx.x + NT * k;
+    const int c4 = idx / CR, l = idx - c4 * CR;
     v[k] = __ldcs(src + static_cast<size_t>(c4) * Lpad + l);
   }
 #pragma unroll
   for (int k = 0; k < PER; ++k) {
-    const int idx = threadIdx.x + 256 * k;
-    const int c4 = idx / 64, l = idx - c4 * 64;
+    const int idx = threadIdx.x + NT * k;
+    const int c4 = idx / CR, l = idx - c4 * CR;
     *reinterpret_cast<float4*>(tile + l * RS + 4 * c4) = v[k];
   }
   __syncthreads();
   constexpr int UPR = D / 8;  // 16-byte output units per row
 #pragma unroll
-  for (int k = 0; k < 64 * UPR / 256; ++k) {
-    const int idx = threadIdx.x + 256 * k;
+  for (int k = 0; k < CR * UPR / NT; ++k) {
+    const int idx = threadIdx.x + NT * k;
     const int l = idx / UPR, u = idx - l * UPR;
     if (l0 + l >= L) continue;
     const float4 a = *reinterpret_cast<const float4*>(tile + l * RS + 8 * u);
