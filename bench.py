@@ -804,11 +804,13 @@ def fp8_arm(args):
     ach = flops / (ms * 1e-3) / 1e12
     burst, sustained, hbm, src = peaks()
     # E4M3 dense tensor rate = 2x the 16-bit rate on this part (4.5 vs 2.25 PFLOP/s nominal).
-    peak = 2.0 * sustained
+    # A kernel of about a millisecond timed alone: the burst figure applies
+    # (sustained beside it), scaled by the nominal E4M3 : BF16 dense ratio of 2.
+    peak = 2.0 * burst
     roof = {"kernel": "fa_fwd_kernel (E4M3)", "bound": "tensor", "achieved": ach, "peak": peak,
             "unit": "TFLOP/s", "frac": ach / peak,
-            "peak_source": f"{src} bf16 sustained x 2 (nominal E4M3 / BF16 dense ratio)",
-            "frac_of_burst": ach / (2.0 * burst), "frac_of_16bit_sustained": ach / sustained,
+            "peak_source": f"{src} bf16 burst x 2 (nominal E4M3 / BF16 dense ratio)",
+            "frac_of_sustained": ach / (2.0 * sustained), "frac_of_16bit_burst": ach / burst,
             "traffic": recorded_traffic("fa_fwd_kernel_e4m3")}
     value = replicas.aggregate_rate(flops, world, ms_per_step * 1e-3) / 1e12
 

@@ -12,14 +12,20 @@ template <int D, bool BF16>
 static fa_status launch_prep(const void* O, const void* dO, float* Delta, float* dq_accum, int B,
                              int L, int H, cudaStream_t s) {
   const int Lpad = padded_len(L);
-  const int grid = B * (Lpad / 32);
-  const size_t smem = static_cast<size_t>(H) * 32 * sizeof(float);
+  // Heads per CTA: all of them when (batch, chunk) pairs alone fill the GPU
+  // twice over, else fewer (halving) until they do.
+  const long long pairs = static_cast<long long>(B) * (Lpad / 32);
+  int hg = H;
+  while (hg > 1 && pairs * ((H + hg - 1) / hg) < 2LL * sm_count()) hg = (hg + 1) / 2;
+  const long long grid = pairs * ((H + hg - 1) / hg);
+  if (grid > 0x7FFFFFFFLL) return FA_ERR_UNSUPPORTED;
+  const size_t smem = static_cast<size_t>(hg) * 32 * sizeof(float);
   auto kern = fa_bwd_prep_kernel<D, BF16>;
   if (smem > 48 * 1024 &&
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
           cudaSuccess)
     return FA_ERR_UNSUPPORTED;
-  kern<<<grid, 256, smem, s>>>(O, dO, Delta, dq_accum, B, L, H, Lpad);
+  kern<<<static_cast<unsigned>(grid), 256, smem, s>>>(O, dO, Delta, dq_accum, B, L, H, Lpad, hg);
   return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 

@@ -746,31 +746,38 @@ __global__ void __launch_bounds__(512, 1)
 }
 
 // ---------------------------------------------------------------- preprocess
-// One CTA per (batch, 32-row chunk of the padded sequence).  Reads the
-// chunk's O and dO rows for every head (one contiguous block), reduces each
-// row in fp32, and writes Delta for each head as 32 contiguous floats.  When
-// an accumulator is given it also zeroes that chunk of it.
+// One CTA per (batch, 32-row chunk of the padded sequence, group of HG
+// heads).  Reads the chunk's O and dO rows of its heads (32 blocks of
+// HG*D contiguous elements), reduces each row in fp32, and writes Delta for
+// each head as 32 contiguous floats.  When an accumulator is given it also
+// zeroes that part of it.  HG is chosen by the launcher so that small
+// batches still give every SM work.
 template <int D, bool BF16>
 __global__ void __launch_bounds__(256)
     fa_bwd_prep_kernel(const void* __restrict__ O, const void* __restrict__ dO,
                        float* __restrict__ Delta, float* __restrict__ dq_accum, int B, int L, int H,
-                       int Lpad) {
+                       int Lpad, int HG) {
   using T = typename std::conditional<BF16, __nv_bfloat16, __half>::type;
   constexpr int TPR = D / 8;  // threads per row (16 bytes each)
-  extern __shared__ float dsm[];  // [H][32]
+  extern __shared__ float dsm[];  // [HG][32]
   const int chunks = Lpad / 32;
-  const int b = blockIdx.x / chunks;
-  const int l0 = (blockIdx.x - b * chunks) * 32;
-  const int nrow = max(0, min(32, L - l0)) * H;  // rows (l, h) with l < L
-  const uint4* o4 = reinterpret_cast<const uint4*>(O) + ((static_cast<size_t>(b) * L + l0) * H) * TPR;
-  const uint4* d4 = reinterpret_cast<const uint4*>(dO) + ((static_cast<size_t>(b) * L + l0) * H) * TPR;
+  const int groups = (H + HG - 1) / HG;
+  const int hg = blockIdx.x % groups;
+  const int bc = blockIdx.x / groups;
+  const int b = bc / chunks;
+  const int l0 = (bc - b * chunks) * 32;
+  const int h0 = hg * HG;
+  const int nh = min(HG, H - h0);                // heads of this group
+  const int nrow = max(0, min(32, L - l0)) * nh;  // rows (l, h) with l < L
   const int sub = threadIdx.x % TPR;
   for (int row = threadIdx.x / TPR; row < ((nrow + (256 / TPR) - 1) / (256 / TPR)) * (256 / TPR);
        row += 256 / TPR) {
     float acc = 0.f;
+    const int l = row / nh, hh = row - l * nh;
     if (row < nrow) {
-      const uint4 a = o4[static_cast<size_t>(row) * TPR + sub];
-      const uint4 c = d4[static_cast<size_t>(row) * TPR + sub];
+      const size_t off = ((static_cast<size_t>(b) * L + l0 + l) * H + h0 + hh) * TPR + sub;
+      const uint4 a = reinterpret_cast<const uint4*>(O)[off];
+      const uint4 c = reinterpret_cast<const uint4*>(dO)[off];
       const T* ea = reinterpret_cast<const T*>(&a);
       const T* ec = reinterpret_cast<const T*>(&c);
 #pragma unroll
@@ -778,25 +785,22 @@ __global__ void __launch_bounds__(256)
     }
 #pragma unroll
     for (int off = TPR / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-    if (sub == 0 && row < nrow) {
-      const int l = row / H, h = row - l * H;
-      dsm[h * 32 + l] = acc;
-    }
+    if (sub == 0 && row < nrow) dsm[hh * 32 + l] = acc;
   }
   __syncthreads();
   const int nl = max(0, min(32, L - l0));
-  for (int idx = threadIdx.x; idx < H * 32; idx += 256) {
-    const int h = idx / 32, l = idx - h * 32;
-    if (l < nl) Delta[(static_cast<size_t>(b) * H + h) * L + l0 + l] = dsm[idx];
+  for (int idx = threadIdx.x; idx < nh * 32; idx += 256) {
+    const int hh = idx / 32, l = idx - hh * 32;
+    if (l < nl) Delta[(static_cast<size_t>(b) * H + h0 + hh) * L + l0 + l] = dsm[idx];
   }
   if (dq_accum) {
     // [B, H, D/4, Lpad, 4]: for each (h, column group) the chunk is 32 float4.
     float4* acc = reinterpret_cast<float4*>(dq_accum);
     const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int idx = threadIdx.x; idx < H * (D / 4) * 32; idx += 256) {
-      const int seg = idx / 32, l = idx - seg * 32;  // seg = h * (D/4) + c4
-      const int h = seg / (D / 4), c4 = seg - h * (D / 4);
-      acc[((static_cast<size_t>(b) * H + h) * (D / 4) + c4) * Lpad + l0 + l] = z;
+    for (int idx = threadIdx.x; idx < nh * (D / 4) * 32; idx += 256) {
+      const int seg = idx / 32, l = idx - seg * 32;  // seg = hh * (D/4) + c4
+      const int hh = seg / (D / 4), c4 = seg - hh * (D / 4);
+      acc[((static_cast<size_t>(b) * H + h0 + hh) * (D / 4) + c4) * Lpad + l0 + l] = z;
     }
   }
 }
