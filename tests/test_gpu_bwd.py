@@ -54,6 +54,23 @@ def test_preprocess_matches_definition(cuda_lib):
         assert torch.count_nonzero(acc).item() == 0, "accumulator not zeroed"
 
 
+@pytest.mark.parametrize("B,L,H,D,dt", [(8, 1024, 5, 64, "fp16"), (1, 1000, 7, 128, "bf16"),
+                                         (2, 77, 3, 64, "fp16"), (1, 4096, 32, 128, "fp16")])
+def test_preprocess_head_groups(cuda_lib, B, L, H, D, dt):
+    """Shapes whose (batch, chunk) pairs alone would not fill the GPU, so the
+    preprocess splits the heads into groups, some of them partial (H = 5, 7)."""
+    g = torch.Generator().manual_seed(B * L + H)
+    dtt = torch.float16 if dt == "fp16" else torch.bfloat16
+    o = torch.randn(B, L, H, D, generator=g).to(dtt)
+    do = torch.randn(B, L, H, D, generator=g).to(dtt)
+    acc = torch.full((fa.workspace_size(B, L, H, D) // 4,), 7.0, device="cuda")
+    delta = fa.bwd_preprocess(o.cuda(), do.cuda(), dq_accum=acc)
+    torch.cuda.synchronize()
+    ref = orc.bwd_preprocess(to64(o), to64(do))
+    assert_close(to64(delta), ref, rtol=1e-5, atol=1e-4, name="Delta")
+    assert torch.count_nonzero(acc).item() == 0, "accumulator not zeroed"
+
+
 def test_smallest_case(cuda_lib):
     run_and_compare(1, 128, 2, 2, 64, "fp16", False, 0)
 
