@@ -67,7 +67,7 @@ struct FwdLayout {
   static constexpr uint32_t BAR_OFF = RING_OFF + STAGES * 2 * TILE;
   // barrier slots
   static constexpr int B_QFULL = 0, B_QEMPTY = 1, B_KVFULL = 2, B_KVEMPTY = 2 + STAGES,
-                       B_SFULL = 2 + 2 * STAGES, B_PFULL = B_SFULL + 2, B_OFULL = B_PFULL + 2,
+                       B_SFULL = 2 + 2 * STAGES, B_PFULL = B_SFULL + 2, B_OFULL = B_PFULL + 4,
                        B_OEMPTY = B_OFULL + 2, B_DONE = B_OEMPTY + 2, NBAR = B_DONE + 1;
   static constexpr uint32_t MISC_OFF = BAR_OFF + NBAR * 8;
   static constexpr uint32_t SMEM_USED = MISC_OFF + 16;
@@ -162,7 +162,9 @@ __global__ void __launch_bounds__(320, 1)
     }
     for (int t = 0; t < 2; ++t) {
       mbar_init(bar(Ly::B_SFULL + t), 1);
-      mbar_init(bar(Ly::B_PFULL + t), 4);  // one arrival per warp of the warpgroup
+      // P of tile t in two halves (keys 0-63, 64-127): one arrival per warp
+      mbar_init(bar(Ly::B_PFULL + 2 * t), 4);
+      mbar_init(bar(Ly::B_PFULL + 2 * t + 1), 4);
       mbar_init(bar(Ly::B_OFULL + t), 1);
       mbar_init(bar(Ly::B_OEMPTY + t), 4);
     }
@@ -278,11 +280,12 @@ __global__ void __launch_bounds__(320, 1)
         }
         __syncwarp();
       };
-      auto issue_pv = [&](int t, uint32_t ps, bool acc) {
+      // PV over the keys of K steps [k_lo, k_hi) of the tile.
+      auto issue_pv = [&](int t, uint32_t ps, bool acc, int k_lo, int k_hi) {
         const uint64_t vd = sdesc_sw128(base + Ly::RING_OFF + 2 * ps * Ly::TILE, Ly::CHUNK, 1024);
         if (elect_one()) {
 #pragma unroll
-          for (int k = 0; k < Ly::KS_PV; ++k) {
+          for (int k = k_lo; k < k_hi; ++k) {
             // P: 8 TMEM columns (16 or 32 keys) per step; V read MN-major.
             const uint64_t off = (Ly::V_STEP * k) >> 4;
             if constexpr (FP8)
@@ -353,13 +356,20 @@ __global__ void __launch_bounds__(320, 1)
                 ok = false;
                 break;
               }
-              if (!mbar_wait_warp(bar(Ly::B_PFULL + t), p_cnt & 1, ab, err, 205)) {
+              // PV on the first half of P while the softmax finishes the second.
+              if (!mbar_wait_warp(bar(Ly::B_PFULL + 2 * t), p_cnt & 1, ab, err, 205)) {
+                ok = false;
+                break;
+              }
+              tc_fence_after();
+              issue_pv(t, ps, j > 0, 0, Ly::KS_PV / 2);
+              if (!mbar_wait_warp(bar(Ly::B_PFULL + 2 * t + 1), p_cnt & 1, ab, err, 207)) {
                 ok = false;
                 break;
               }
               ++p_cnt;
               tc_fence_after();
-              issue_pv(t, ps, j > 0);
+              issue_pv(t, ps, true, Ly::KS_PV / 2, Ly::KS_PV);
               if (j == it.n[t] - 1) {
                 commit(Ly::B_OFULL + t);
                 ++o_uses;
@@ -421,18 +431,20 @@ __global__ void __launch_bounds__(320, 1)
           for (int c = 0; c < 128; ++c)
             if (k0 + c >= lim) sr[c] = __float_as_uint(-INFINITY);
         }
-        // The row max runs as four independent chains of three-input max
-        // operations (key 4w+u in chain u) instead of 128 dependent ones.
-        float mx4[4];
+        // The row max runs as eight independent chains of three-input max
+        // operations (key 8w+u in chain u, 16 keys each) instead of 128
+        // dependent ones, then combines the chains.
+        float mx8[8];
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          mx4[u] = __uint_as_float(sr[u]);
+        for (int u = 0; u < 8; ++u) {
+          mx8[u] = fmax3(__uint_as_float(sr[u]), __uint_as_float(sr[8 + u]), __uint_as_float(sr[16 + u]));
 #pragma unroll
-          for (int w = 1; w < 31; w += 2)
-            mx4[u] = fmax3(mx4[u], __uint_as_float(sr[4 * w + u]), __uint_as_float(sr[4 * w + 4 + u]));
-          mx4[u] = fmaxf(mx4[u], __uint_as_float(sr[124 + u]));
+          for (int w = 3; w < 15; w += 2)
+            mx8[u] = fmax3(mx8[u], __uint_as_float(sr[8 * w + u]), __uint_as_float(sr[8 * w + 8 + u]));
+          mx8[u] = fmaxf(mx8[u], __uint_as_float(sr[120 + u]));
         }
-        const float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
+        const float mx = fmax3(fmax3(mx8[0], mx8[1], mx8[2]), fmax3(mx8[3], mx8[4], mx8[5]),
+                               fmaxf(mx8[6], mx8[7]));
         const float m_new = fmaxf(m, mx);
         float alpha = 1.f;
         bool rescale = false;
@@ -445,6 +457,29 @@ __global__ void __launch_bounds__(320, 1)
           m = m_new;
           rescale = true;
         }
+        // Half h of P is in TMEM: this thread's stores complete, then one
+        // lane per warp signals the MMA warp.  Before the first half, O of
+        // this row is scaled by alpha if the max moved (this tile's PV
+        // accumulates into it next; the previous PV has completed, as the
+        // commit that signalled this tile's S covers it).  That happens once
+        // the first half's scores are spent, so their registers hold O.
+        auto p_ready = [&](int h) {
+          if (h == 0 && rescale) {
+#pragma unroll
+            for (int cc = 0; cc < D / 32; ++cc) {
+              uint32_t o[32];
+              tmem_ld32(tO + 32 * cc, o);
+              tmem_ld_wait32(o);
+#pragma unroll
+              for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+              tmem_st32(tO + 32 * cc, o);
+            }
+          }
+          tmem_st_wait();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar(Ly::B_PFULL + 2 * t + h));
+        };
         const float mb = m * sl2;
         float rs = 0.f;
         if constexpr (FP8) {
@@ -467,6 +502,7 @@ __global__ void __launch_bounds__(320, 1)
               pk[i] = pack4_e4m3(p0, p1, p2, p3);
             }
             tmem_st16(tS + 16 * h2, pk);
+            p_ready(h2);
           }
           float rs4[4];
 #pragma unroll
@@ -494,6 +530,7 @@ __global__ void __launch_bounds__(320, 1)
               pk[i] = pack2<T>(p0, p1);
             }
             tmem_st16(tS + 16 * q4, pk);
+            if (q4 & 1) p_ready(q4 >> 1);
           }
           float rs4[4];
 #pragma unroll
@@ -504,27 +541,7 @@ __global__ void __launch_bounds__(320, 1)
           }
           rs = (rs4[0] + rs4[1]) + (rs4[2] + rs4[3]);
         }
-        if (rescale) {
-          // O of this row scaled by alpha before this tile's PV accumulates
-          // into it.  PV of the previous tile has completed: the commit that
-          // signalled this tile's S covers it.
-#pragma unroll
-          for (int cc = 0; cc < D / 32; ++cc) {
-            uint32_t o[32];
-            tmem_ld32(tO + 32 * cc, o);
-            tmem_ld_wait32(o);
-#pragma unroll
-            for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-            tmem_st32(tO + 32 * cc, o);
-          }
-        }
         l = l * alpha + rs;
-        // P (and any O rescale) is in TMEM: this thread's stores complete,
-        // then one lane per warp signals the MMA warp.
-        tmem_st_wait();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar(Ly::B_PFULL + t));
       }
       if (!ok) break;
       // ---- epilogue: O / l, LSE
