@@ -20,6 +20,7 @@ from __future__ import annotations
 
 import argparse
 import csv
+import datetime
 import hashlib
 import io
 import json
@@ -141,17 +142,20 @@ def recorded_traffic(kernel):
 # --------------------------------------------------------------------- clocks
 
 class ClockSampler:
-    """nvidia-smi sampled every 100 ms while the timed region runs."""
+    """nvidia-smi sampled every 20 ms; only samples stamped inside the timed
+    region (between start() returning and stop() being called) count."""
 
-    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    QUERY = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    PERIOD_MS = 20
 
     def __init__(self, gpu_index, enabled=True):
         self.gpu = gpu_index
         self.enabled = enabled
         self.proc = None
         self.tmp = None
+        self.t0 = None
 
     def start(self):
         if not self.enabled:
@@ -160,17 +164,55 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.QUERY}",
-                 "--format=csv,noheader,nounits", "-lms", "100"],
+                 "--format=csv,noheader,nounits", "-lms", str(self.PERIOD_MS)],
                 stdout=self.tmp, stderr=subprocess.DEVNULL)
         except OSError:
             self.proc = None
         time.sleep(0.3)
+        self.t0 = datetime.datetime.now()
+
+    @staticmethod
+    def summarize(rows, t0, t1):
+        """Median SM clock, peak clock and active throttle reasons of the rows
+        (nvidia-smi CSV, timestamp first) stamped within [t0, t1]."""
+        sm, mx, pw, reasons, total = [], [], [], set(), 0
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            if len(r) < 10:
+                continue
+            try:
+                ts = datetime.datetime.strptime(r[0].strip(), "%Y/%m/%d %H:%M:%S.%f")
+                clk, cmax = float(r[2]), float(r[3])
+            except ValueError:
+                continue
+            total += 1
+            if not (t0 <= ts <= t1):
+                continue
+            sm.append(clk)
+            mx.append(cmax)
+            try:
+                pw.append(float(r[4]))
+            except ValueError:
+                pass
+            for name, val in zip(names, r[6:10]):
+                if val.strip().lower() == "active":
+                    reasons.add(name)
+        out = {"sm_mhz": statistics.median(sm) if sm else None,
+               "sm_max_mhz": max(mx) if mx else None,
+               "reasons": sorted(reasons), "samples": len(sm), "samples_outside": total - len(sm)}
+        if pw:
+            out["power_w_median"] = statistics.median(pw)
+        if not sm:
+            out["reasons"] = ["no sample inside the timed region"]
+        return out
 
     def stop(self):
         if not self.enabled:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["not sampled"]}
         if self.proc is None:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        t1 = datetime.datetime.now()
+        time.sleep(3 * self.PERIOD_MS / 1000.0)
         self.proc.terminate()
         try:
             self.proc.wait(timeout=5)
@@ -178,22 +220,9 @@ class ClockSampler:
             self.proc.kill()
         self.tmp.flush()
         self.tmp.seek(0)
-        rows = [r for r in csv.reader(io.StringIO(self.tmp.read())) if len(r) >= 9]
+        rows = list(csv.reader(io.StringIO(self.tmp.read())))
         os.unlink(self.tmp.name)
-        sm, mx, reasons = [], [], set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for r in rows:
-            try:
-                sm.append(float(r[1]))
-                mx.append(float(r[2]))
-            except ValueError:
-                continue
-            for name, val in zip(names, r[5:9]):
-                if val.strip().lower() == "active":
-                    reasons.add(name)
-        return {"sm_mhz": statistics.median(sm) if sm else None,
-                "sm_max_mhz": max(mx) if mx else None,
-                "reasons": sorted(reasons), "samples": len(sm)}
+        return self.summarize(rows, self.t0, t1)
 
 
 # --------------------------------------------------------------------- oracle timing

@@ -79,3 +79,25 @@ def test_source_hash_covers_the_kernel_sources(kernel, monkeypatch, tmp_path):
     last = tmp_path / bench.KERNEL_SOURCES[kernel][-1]
     last.write_text(last.read_text() + "\n// edit\n")
     assert bench.source_hash(kernel) != before
+
+
+def test_clock_samples_count_only_inside_the_timed_region():
+    import datetime
+    t0 = datetime.datetime(2026, 1, 1, 12, 0, 0)
+    t1 = t0 + datetime.timedelta(seconds=1)
+    idle = ["Not Active"] * 4
+    capped = ["Not Active"] * 3 + ["Active"]
+    rows = [
+        ["2026/01/01 11:59:59.900", "0", "2070", "2070", "300", "0x0"] + idle,   # before
+        ["2026/01/01 12:00:00.200", "0", "1700", "2070", "1390", "0x4"] + capped,
+        ["2026/01/01 12:00:00.600", "0", "1750", "2070", "1395", "0x4"] + capped,
+        ["2026/01/01 12:00:00.900", "0", "1800", "2070", "1380", "0x4"] + capped,
+        ["2026/01/01 12:00:01.300", "0", "2070", "2070", "350", "0x0"] + idle,   # after
+        ["garbled"],
+    ]
+    c = bench.ClockSampler.summarize(rows, t0, t1)
+    assert c["sm_mhz"] == 1750.0 and c["samples"] == 3 and c["samples_outside"] == 2
+    assert c["reasons"] == ["sw_power_cap"] and c["sm_max_mhz"] == 2070.0
+    # a region with no sample inside says so instead of quoting idle clocks
+    c = bench.ClockSampler.summarize(rows[:1], t0, t1)
+    assert c["sm_mhz"] is None and c["reasons"] == ["no sample inside the timed region"]
