@@ -90,6 +90,28 @@ def test_large_scores_stay_finite(cuda_lib):
         assert_close(to64(lse), rl, rtol=1e-5, atol=LSE_ATOL, name="LSE")
 
 
+@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("dtype", [torch.float16, torch.bfloat16])
+@pytest.mark.parametrize("causal", [False, True])
+def test_row_max_rising_every_tile(cuda_lib, D, dtype, causal):
+    """Scores that rise by ~20 (natural log) across every 128-key tile: every
+    row's running max grows past the 2^8 rescale threshold at each K/V tile,
+    always at the tile's last keys, so O is rescaled at every step (after
+    the first half of P is stored and before the tensor core adds PV)."""
+    B, L, H = 1, 640, 2
+    g = torch.Generator().manual_seed(21)
+    alpha = 20.0 / (128 * D ** 0.5)  # score rise per key: q . k_j / sqrt(D) ~ sqrt(D) * alpha * j
+    ramp = alpha * torch.arange(L, dtype=torch.float32).view(1, L, 1, 1)
+    q = (1 + 0.1 * torch.randn(B, L, H, D, generator=g)).to(dtype)
+    k = (ramp * (1 + 0.1 * torch.randn(B, L, H, D, generator=g))).to(dtype)
+    v = torch.randn(B, L, H, D, generator=g).to(dtype)
+    o, lse = fa.fwd(q.cuda(), k.cuda(), v.cuda(), causal)
+    ro, rl = orc.forward(to64(q), to64(k), to64(v), causal)
+    assert np.isfinite(to64(o)).all()
+    assert_close(to64(o), ro, name="O")
+    assert_close(to64(lse), rl, rtol=1e-5, atol=LSE_ATOL, name="LSE")
+
+
 def test_repeated_calls_are_deterministic(cuda_lib):
     (_, _, _, _), (qd, kd, vd, _) = inputs(2, 700, 4, 2, 128, "bf16", 11)
     o1, l1 = fa.fwd(qd, kd, vd, True)
