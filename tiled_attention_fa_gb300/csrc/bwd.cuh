@@ -85,6 +85,7 @@ struct BwdParams {
   int n_items;  // B * Hkv * n_kv
   int n_units;  // work units of the persistent CTAs (see bwd_unit_item)
   int ipu;      // K/V tiles per unit: 2 under causal masking, else 1
+  int snake;    // 1: units are single tiles in decreasing-work order, dealt out in snake order
   float sl2;    // log2(e) / sqrt(D)
   float scale;  // 1 / sqrt(D)
 };
@@ -180,7 +181,22 @@ __device__ __forceinline__ BwdItem bwd_decode(int item, const BwdParams& p) {
 // Units of one head are consecutive, so the CTAs running at the same time
 // share a few heads' Q / dO in L2.  Returns false for the missing second tile
 // of the middle pair when n_kv is odd.
+// A causal problem of only a few rounds (snake = 1) balances better with
+// single tiles instead: sorted by decreasing work (tile j before j+1, all
+// heads), round r of the CTAs takes the next gridDim.x of them, CTA c the c-th
+// in even rounds and the (gridDim.x-1-c)-th in odd ones.  The CTAs' loops
+// then run over rounds x gridDim.x units; positions past the tiles are empty.
 __device__ __forceinline__ bool bwd_unit_item(int u, int s, const BwdParams& p, int& item) {
+  if (p.snake) {
+    const int G = static_cast<int>(gridDim.x);
+    const int r = u / G, c = u - r * G;
+    const int k = r * G + ((r & 1) ? G - 1 - c : c);
+    if (k >= p.n_items) return false;
+    const int nbh = p.n_items / p.n_kv;
+    const int j = k / nbh;
+    item = (k - j * nbh) * p.n_kv + j;
+    return true;
+  }
   if (p.ipu == 1) {
     item = u;
     return true;
