@@ -46,6 +46,7 @@ struct FwdParams {
   int n_items;   // B * H * n_qpairs
   float sl2;     // log2(e) / sqrt(D) (times q_scale * k_scale for E4M3 inputs)
   float o_scale; // factor on O / l at the store: 1, or v_scale for E4M3 inputs
+  int sorted;    // 1: items ordered by decreasing work across all heads (else head-major)
 };
 
 // FP8: Q, K, V are E4M3 codes (one byte per element; D = 128 only).
@@ -92,9 +93,20 @@ struct FwdItem {
 
 __device__ __forceinline__ FwdItem fwd_decode(int item, const FwdParams& p) {
   FwdItem it;
-  const int bh = item / p.n_qpairs;
-  // Within a head, pairs run from the last (longest under causal) to the first.
-  const int qp = p.n_qpairs - 1 - (item - bh * p.n_qpairs);
+  int bh, qp;
+  if (p.sorted) {
+    // Pair index falling (work falling under causal masking), all heads of
+    // one pair index together.
+    const int nbh = p.n_items / p.n_qpairs;
+    const int r = item / nbh;
+    bh = item - r * nbh;
+    qp = p.n_qpairs - 1 - r;
+  } else {
+    // Head-major; within a head, pairs run from the last (longest under
+    // causal) to the first.
+    bh = item / p.n_qpairs;
+    qp = p.n_qpairs - 1 - (item - bh * p.n_qpairs);
+  }
   it.b = bh / p.H;
   it.h = bh - it.b * p.H;
   it.hkv = it.h / (p.H / p.Hkv);
